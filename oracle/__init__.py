@@ -1,0 +1,157 @@
+"""ctypes shim over the CPU oracle (``mhc_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline / reference leg load this; the library never does.  It shares no
+code with the CUDA path; the only thing both sides share is the seeded input
+generator, which holds none of the op's arithmetic.
+
+Parity pins: every oracle function is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` (closed forms, invariants, special cases that
+reduce to a library routine, hand-derived worked examples under
+``tests/golden/``).  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mhc_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libmhc_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain -O2, no fast-math) into oracle/_build/."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall",
+                               "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64, D, I = ctypes.c_int64, ctypes.c_double, ctypes.c_int
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = D
+            lib.oracle_double_to_bf16.argtypes = [D]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_sinkhorn.argtypes = [P, I, D]
+            lib.oracle_sinkhorn.restype = None
+            lib.oracle_post.argtypes = [P, P, P, P, I64, I64, P, I]
+            lib.oracle_post.restype = I
+            lib.oracle_pre.argtypes = [P, P, P, P, P, I64, I64, D, D, D, D, I,
+                                       P, P, P, P, P, P, P, I]
+            lib.oracle_pre.restype = I
+            lib.oracle_shifted_post_pre.argtypes = [P, P, P, P, P, P, P, P, I64, I64,
+                                                    D, D, D, D, I, P, P, P, P, P, P, P, P, I]
+            lib.oracle_shifted_post_pre.restype = I
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def bf16_to_double(b: int) -> float:
+    return _load().oracle_bf16_to_double(int(b))
+
+
+def double_to_bf16(x: float) -> int:
+    return int(_load().oracle_double_to_bf16(float(x)))
+
+
+def sinkhorn(M, iters: int, eps: float) -> np.ndarray:
+    m = np.array(M, dtype=np.float64).reshape(16).copy()
+    _load().oracle_sinkhorn(_p(m), int(iters), float(eps))
+    return m.reshape(4, 4)
+
+
+def post(R, Y, prev_post, prev_comb, nthreads: int | None = None):
+    R = _c(R, np.uint16); Y = _c(Y, np.uint16)
+    T, _, H = R.shape
+    pp = _c(prev_post, np.float32); pc = _c(prev_comb, np.float32)
+    out = np.empty_like(R)
+    rc = _load().oracle_post(_p(R), _p(Y), _p(pp), _p(pc), T, H, _p(out),
+                             nthreads or default_threads())
+    assert rc == 0
+    return out
+
+
+def _sc(kw):
+    return (float(kw["hc_norm_eps"]), float(kw["rmsnorm_eps"]), float(kw["hc_post_scale"]),
+            float(kw["sinkhorn_eps"]), int(kw["sinkhorn_iters"]))
+
+
+def pre(Rp, phi, bias, mix_scales, gamma, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,
+        sinkhorn_eps, sinkhorn_iters, nthreads: int | None = None, debug: bool = False):
+    """Steps (2)-(4).  Returns dict with X (bf16 bits), pre, post, res (fp64) [+ z, r, rstd]."""
+    Rp = _c(Rp, np.uint16)
+    T, _, H = Rp.shape
+    phi = _c(phi, np.float32); bias = _c(bias, np.float32)
+    ms = _c(mix_scales, np.float32); g = _c(gamma, np.uint16)
+    X = np.empty((T, H), np.uint16)
+    pre_ = np.empty((T, 4)); post_ = np.empty((T, 4)); res = np.empty((T, 4, 4))
+    z = np.empty((T, 24)) if debug else None
+    r = np.empty(T) if debug else None
+    rstd = np.empty(T) if debug else None
+    rc = _load().oracle_pre(_p(Rp), _p(phi), _p(bias), _p(ms), _p(g), T, H,
+                            *_sc(dict(hc_norm_eps=hc_norm_eps, rmsnorm_eps=rmsnorm_eps,
+                                      hc_post_scale=hc_post_scale, sinkhorn_eps=sinkhorn_eps,
+                                      sinkhorn_iters=sinkhorn_iters)),
+                            _p(X), _p(pre_), _p(post_), _p(res), _p(z), _p(r), _p(rstd),
+                            nthreads or default_threads())
+    assert rc == 0
+    out = dict(X=X, pre=pre_, post=post_, res=res)
+    if debug:
+        out.update(z=z, r=r, rstd=rstd)
+    return out
+
+
+def shifted_post_pre(R, Y, prev_post, prev_comb, phi, bias, mix_scales, gamma, *,
+                     hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters,
+                     nthreads: int | None = None, debug: bool = False, want_R: bool = True):
+    """The whole step.  Returns dict with R (bf16 bits), X, pre, post, res [+ z, r, rstd]."""
+    R = _c(R, np.uint16); Y = _c(Y, np.uint16)
+    T, _, H = R.shape
+    pp = _c(prev_post, np.float32); pc = _c(prev_comb, np.float32)
+    phi = _c(phi, np.float32); bias = _c(bias, np.float32)
+    ms = _c(mix_scales, np.float32); g = _c(gamma, np.uint16)
+    Rout = np.empty_like(R) if want_R else None
+    X = np.empty((T, H), np.uint16)
+    pre_ = np.empty((T, 4)); post_ = np.empty((T, 4)); res = np.empty((T, 4, 4))
+    z = np.empty((T, 24)) if debug else None
+    r = np.empty(T) if debug else None
+    rstd = np.empty(T) if debug else None
+    rc = _load().oracle_shifted_post_pre(
+        _p(R), _p(Y), _p(pp), _p(pc), _p(phi), _p(bias), _p(ms), _p(g), T, H,
+        *_sc(dict(hc_norm_eps=hc_norm_eps, rmsnorm_eps=rmsnorm_eps, hc_post_scale=hc_post_scale,
+                  sinkhorn_eps=sinkhorn_eps, sinkhorn_iters=sinkhorn_iters)),
+        _p(Rout), _p(X), _p(pre_), _p(post_), _p(res), _p(z), _p(r), _p(rstd),
+        nthreads or default_threads())
+    assert rc == 0
+    out = dict(R=Rout, X=X, pre=pre_, post=post_, res=res)
+    if debug:
+        out.update(z=z, r=r, rstd=rstd)
+    return out
