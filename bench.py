@@ -1,0 +1,313 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused mHC post+pre step (mhc_shifted_post_pre) on GB300.
+
+One step = one call of the whole op (post, RMS + projection, heads + Sinkhorn,
+combine + RMSNorm) over the prefill-chunk workload: T=8192 tokens, H=7168,
+hc_mult=4, seeded synthetic inputs already resident in HBM.  Prints one JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 C implementation used by
+the tests) on the host cores over a bounded token sample of the same workload.
+Under torchrun with N > 1 every rank runs an independent replica on its own GPU
+(the op has no exchange step: tokens are independent), and value is the total
+over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import platform
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from manifold_constrained_hyper_mhc_gb300 import synth  # noqa: E402
+
+WORKLOAD = "prefill_chunk"
+METRIC = "tokens/s and HBM GB/s (% of GB300 peak) for fused mHC post+pre vs T, H"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(T: int, H: int) -> int:
+    """Bytes the op must move per call: per token R 8H + Y 2H + prev mixes 80 B in,
+    R' 8H + layer input 2H + mixes 96 B out; per call phi 96H + gamma 2H + bias and
+    mix scales 108 B."""
+    return T * (20 * H + 176) + 96 * H + 2 * H + 108
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        rows = [r for r in self.rows if len(r) >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.nanmedian(sm)), "sm_max_mhz": num(rows[0][1]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": float(np.nanmax([num(r[2]) for r in rows]))}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0, None
+    import torch
+    import torch.distributed as dist
+    rank, lr = int(os.environ["RANK"]), int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(lr)
+    dist.init_process_group(backend)
+    return rank, ws, lr, dist
+
+
+def time_oracle(w, phi, bias, ms, gamma, n_tokens, min_seconds, t_offset=0):
+    """Times the CPU oracle over n_tokens tokens of the workload, repeated until
+    min_seconds have passed.  Returns (tokens/s, threads, seconds, tokens)."""
+    import oracle
+    oracle.build()
+    t0 = t_offset % max(1, w.T - n_tokens + 1)
+    R, Y, pp, pc = synth.tokens(w, t0, t0 + n_tokens)
+    nt = oracle.default_threads()
+    done, start = 0, time.perf_counter()
+    while True:
+        oracle.shifted_post_pre(R, Y, pp, pc, phi, bias, ms, gamma, **synth.scalars(), nthreads=nt)
+        done += n_tokens
+        el = time.perf_counter() - start
+        if el >= min_seconds:
+            return done / el, nt, el, done
+
+
+def run_reference(args, rank, world, dist):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[WORKLOAD]
+    phi, bias, ms, gamma = synth.weights(w)
+    n = 512
+    times = []
+    for s in range(args.warmup + args.steps):
+        tps, nt, el, done = time_oracle(w, phi, bias, ms, gamma, n, 0.0, t_offset=s * n)
+        if s >= args.warmup:
+            times.append(el)
+    ms_step = 1e3 * float(np.mean(times))
+    value = n / (ms_step / 1e3)
+    sample = f"{n} consecutive tokens of the {WORKLOAD} workload (T={w.T}, H={w.H}) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} T={w.T} H={w.H} hc_mult=4", "T": w.T, "H": w.H,
+                   "tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
+                         "machine": platform.machine()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, lr, dist):
+    import torch
+    import manifold_constrained_hyper_mhc_gb300 as mhc
+    from manifold_constrained_hyper_mhc_gb300 import _build
+    _build.build()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    dev = torch.device("cuda", lr if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[WORKLOAD]
+    T, H = w.T, w.H
+    phi, bias, msc, gamma = synth.weights(w)
+    R, Y, pp, pc = synth.tokens(w)
+
+    def d_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    Rd, Yd = d_bf16(R), d_bf16(Y)
+    ppd, pcd = torch.from_numpy(pp).to(dev), torch.from_numpy(pc).to(dev)
+    wd = (torch.from_numpy(phi).to(dev), torch.from_numpy(bias).to(dev), torch.from_numpy(msc).to(dev),
+          d_bf16(gamma))
+    sc = synth.scalars()
+    ws = mhc.new_workspace(T, H, dev)
+    out = {"residual_out": torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev),
+           "layer_in": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+           "pre_mix": torch.empty((T, 4), device=dev), "post_mix": torch.empty((T, 4), device=dev),
+           "comb_res_mix": torch.empty((T, 4, 4), device=dev)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    launches = mhc.last_launch_count()
+    torch.cuda.synchronize(dev)
+    mhc.check_status(ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    el_ms = ev0.elapsed_time(ev1)
+    mhc.check_status(ws)
+    if dist is not None:
+        t = torch.tensor([el_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el_ms = float(t.item())
+    ms_step = el_ms / args.steps
+    value = world * T / (ms_step / 1e3)
+
+    # e2e through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the call, D2H of its outputs, every step.
+    hR = torch.from_numpy(R.view(np.int16)).pin_memory()
+    hY = torch.from_numpy(Y.view(np.int16)).pin_memory()
+    hpp, hpc = torch.from_numpy(pp).pin_memory(), torch.from_numpy(pc).pin_memory()
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in (hR, hY, hpp, hpc))
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    bufR, bufY = torch.empty_like(Rd), torch.empty_like(Yd)
+    bufpp, bufpc = torch.empty_like(ppd), torch.empty_like(pcd)
+
+    def e2e_step():
+        bufR.view(torch.int16).copy_(hR, non_blocking=True)
+        bufY.view(torch.int16).copy_(hY, non_blocking=True)
+        bufpp.copy_(hpp, non_blocking=True)
+        bufpc.copy_(hpc, non_blocking=True)
+        mhc.shifted_post_pre(bufR, bufY, bufpp, bufpc, *wd, **sc, out=out, workspace=ws, stream=stream)
+        for k, v in out.items():
+            hout[k].copy_(v, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    peak, peak_src = peaks()
+    abytes = algorithmic_bytes(T, H)
+    achieved = abytes / (ms_step / 1e3) / 1e9
+    sched = {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} T={T} H={H} hc_mult=4", "T": T, "H": H, "io": "bf16 streams, fp32 mixes",
+                   "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
+                   "hbm_gbs": achieved, "hbm_frac": achieved / peak},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": f"whole call ({launches} launches), algorithmic bytes {abytes}"},
+        "gpu_launches": launches * args.steps,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tps, nt, el, done = time_oracle(w, phi, bias, msc, gamma, 1024, 10.0)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                                "sample": f"first 1024 tokens of {WORKLOAD} (T={T}, H={H}), repeated for "
+                                          f"{el:.1f} s ({done} tokens)", "machine": platform.machine()}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, lr, dist = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, dist)
+        else:
+            run_ours(args, rank, world, lr, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * mhc.h -- C ABI of the GB300 (sm_103a) fused mHC post+pre library (libmhc.so).
+ *
+ * The op.  A DeepSeek-V4-style decoder carries hc_mult = 4 residual streams per
+ * token.  At every layer boundary the previous layer's output is folded into
+ * the streams ("post") and the next layer's input is formed from them ("pre").
+ * The pages this follows:
+ *   - "[SM80] Backport mHC fused post + int8 all-reduce; fixes #28, #29",
+ *     "What this fixes": the mHC post kernel and its fused square sum.
+ *   - "[DSv4.1] Integrate Mega-mHC from DeepGEMM": the fused post+pre op
+ *     mhc_shifted_post_pre (Mega-mHC), its scalar tail and naming
+ *     ("Style findings", Major 1: rms_eps->hc_norm_eps, hc_post_alpha->
+ *     hc_post_scale, norm_eps->rmsnorm_eps, res_mix->comb_res_mix), the
+ *     distinct eps values that catch an argument swap ("Verified OK"), the
+ *     hc_mult == 4 gate and the 2^20 token bound ("Verified OK"), and the
+ *     capture-on-a-fresh-stream hazard of lazily created barrier state
+ *     ("Correctness findings", Minor 3).
+ *   - "[DSV4.1] Four BS=1 critical-path fixes for DSpark decode": the mHC
+ *     statistics and Sinkhorn and the combine+RMSNorm ("What changed" item 3,
+ *     "Measured and deliberately left out").
+ *
+ * Per token t (all tokens are independent), with streams R[t] in [4][H]:
+ *   (1) post:    R'[i] = sum_j comb[j][i] * R[j] + post[i] * Y           -> bf16
+ *   (2) RMS:     r = 1 / sqrt(mean over the 4H entries of R'^2 + hc_norm_eps)
+ *                z = r * (flat(R') @ phi),  flat index k = i*H + h,  24 logits
+ *   (3) heads:   pre_mix[i]  = sigmoid(alpha_pre  * z[i]   + bias[i])
+ *                post_mix[i] = hc_post_scale * sigmoid(alpha_post * z[4+i] + bias[4+i])
+ *                comb_res_mix = Sinkhorn(M),  M[a][c] = exp(alpha_res * z[8+4a+c] + bias[8+4a+c]),
+ *                  one iteration = rows /= (row sum + sinkhorn_eps), then
+ *                  columns /= (column sum + sinkhorn_eps); sinkhorn_iters iterations
+ *   (4) combine: X = sum_i pre_mix[i] * R'[i];  out = X / sqrt(mean_h X^2 + rmsnorm_eps) * gamma -> bf16
+ * Steps (2)-(4) consume the bf16-rounded R', so mhc_shifted_post_pre equals
+ * mhc_post followed by mhc_pre bit for bit.  comb_res_mix_out is written
+ * [a][c] and a following call consumes it as prev_comb_res_mix[j][i].
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is a DEVICE pointer, owned by the caller, row-major and
+ *     contiguous, 16-byte aligned.  bf16 data is passed as raw bit patterns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  They never synchronise, never allocate, and keep no lazy per-
+ *     stream state, so the first call may happen inside CUDA-graph capture.
+ *   - Arguments are validated before anything is launched; on any error nothing
+ *     is launched and no output is touched.
+ *   - T == 0 is valid and launches nothing.  1 <= T <= MHC_MAX_TOKENS,
+ *     8 <= H <= MHC_MAX_HIDDEN, H % 8 == 0 (16-byte bf16 vectors).
+ *   - The eps values must be finite and >= 0, hc_post_scale finite,
+ *     0 <= sinkhorn_iters <= MHC_MAX_SINKHORN_ITERS.
+ *   - residual_out may be the same buffer as residual (in-place update); any
+ *     other overlap between an input and an output is rejected.
+ *   - The workspace is caller-owned device memory of at least
+ *     mhc_workspace_size(T, H) bytes, 256-byte aligned.  Before its first use it
+ *     must be zero-filled (e.g. cudaMemsetAsync); every successful call leaves
+ *     it zeroed-state-compatible again.  Calls that share one workspace must be
+ *     ordered (same stream or explicit events); concurrent use races.
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MHC_API __attribute__((visibility("default")))
+#else
+#define MHC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mhc_bf16; /* bfloat16 bit pattern */
+
+#define MHC_HC_MULT 4
+#define MHC_NUM_MIX 24
+#define MHC_MAX_TOKENS (1 << 22)
+#define MHC_MAX_HIDDEN 65536
+#define MHC_MAX_SINKHORN_ITERS 64
+
+typedef enum mhc_status {
+    MHC_OK = 0,
+    MHC_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size, bad scalar, overlap */
+    MHC_ERR_UNSUPPORTED = -2,    /* device is not sm_103 / forced schedule cannot run this shape */
+    MHC_ERR_WORKSPACE = -3,      /* workspace missing, too small or misaligned */
+    MHC_ERR_CUDA = -4,           /* a CUDA runtime call or launch failed (see mhc_last_error) */
+    MHC_ERR_DEVICE_TIMEOUT = -5  /* a bounded device-side wait gave up (mhc_check_status) */
+} mhc_status;
+
+/* Kernel schedules.  AUTO picks by T, H and the SM count. */
+typedef enum mhc_schedule {
+    MHC_SCHEDULE_AUTO = 0,
+    MHC_SCHEDULE_SPLIT = 1   /* three launches: post + partial sums, mixes, combine + RMSNorm */
+} mhc_schedule;
+
+/* Bytes of workspace the calls below need for T tokens of hidden size H. */
+MHC_API size_t mhc_workspace_size(int64_t T, int64_t H);
+
+/* The fused step (1)-(4): mhc_shifted_post_pre / Mega-mHC ("[DSv4.1] Integrate
+ * Mega-mHC from DeepGEMM", "Purpose" and "Verified OK").
+ *   residual          [T,4,H] bf16   streams before this layer's post
+ *   layer_out         [T,H]   bf16   the previous sublayer's output Y
+ *   prev_post_mix     [T,4]   fp32   post mix of the previous layer
+ *   prev_comb_res_mix [T,4,4] fp32   residual mix of the previous layer, [j][i]
+ *   phi               [4H,24] fp32   projection, row k = i*H + h
+ *   bias              [24]    fp32   0:4 pre, 4:8 post, 8:24 residual mix (row-major 4x4)
+ *   mix_scales        [3]     fp32   alpha_pre, alpha_post, alpha_res
+ *   rmsnorm_weight    [H]     bf16   gamma
+ * Outputs:
+ *   residual_out      [T,4,H] bf16   R'
+ *   layer_in_out      [T,H]   bf16   RMSNorm(sum_i pre_mix[i] R'[i]) * gamma
+ *   pre_mix_out       [T,4]   fp32
+ *   post_mix_out      [T,4]   fp32
+ *   comb_res_mix_out  [T,4,4] fp32   [a][c]
+ * The scalar tail is in this order: hc_norm_eps, rmsnorm_eps, hc_post_scale,
+ * sinkhorn_eps, sinkhorn_iters. */
+MHC_API mhc_status mhc_shifted_post_pre(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,
+    const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps,
+    float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Step (1) alone: the mHC post ("[SM80] Backport mHC fused post + int8
+ * all-reduce", "What this fixes").  Needs no workspace. */
+MHC_API mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                    const float *prev_post_mix, const float *prev_comb_res_mix, int64_t T,
+                    int64_t H, mhc_bf16 *residual_out, void *stream);
+
+/* Steps (2)-(4) alone: the mHC pre, from streams that already went through the
+ * post (`residual` here is R').  Same arguments and outputs as the fused call. */
+MHC_API mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const float *bias,
+                   const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T,
+                   int64_t H, float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                   float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *layer_in_out,
+                   float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Forces a schedule for every following call of this process (a test hook; the
+ * default is MHC_SCHEDULE_AUTO).  Returns MHC_ERR_INVALID_ARG for an unknown value. */
+MHC_API mhc_status mhc_set_schedule(int schedule);
+
+/* The schedule AUTO would pick for (T, H) on the current device. */
+MHC_API int mhc_auto_schedule(int64_t T, int64_t H);
+
+/* Synchronises `stream`, then reads and clears the device status word kept in
+ * the workspace: MHC_ERR_DEVICE_TIMEOUT if a bounded device-side wait gave up
+ * since the last check (the workspace must then be zero-filled again),
+ * MHC_ERR_CUDA if the stream reports an error, else MHC_OK. */
+MHC_API mhc_status mhc_check_status(void *workspace, void *stream);
+
+/* Number of kernels launched by the last call on this thread (0 if it failed
+ * or launched nothing). */
+MHC_API int mhc_last_launch_count(void);
+
+/* Static description of a status code; never NULL. */
+MHC_API const char *mhc_status_string(int status);
+
+/* Detail of the last MHC_ERR_CUDA / MHC_ERR_INVALID_ARG on this thread (never NULL). */
+MHC_API const char *mhc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_H */

@@ -1,0 +1,214 @@
+"""Python binding of libmhc.so, the GB300 fused mHC post+pre library.
+
+Argument marshalling only: every step of the op runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  The library must be
+built (``_build.build()``); importing the binding without it, or calling it
+without a CUDA device, raises -- there is no CPU fallback.
+
+Names follow the C ABI in ``include/mhc.h`` (mhc_shifted_post_pre, mhc_post,
+mhc_pre), which follows "[DSv4.1] Integrate Mega-mHC from DeepGEMM".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
+    "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
+]
+
+OK = 0
+STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
+          -4: "MHC_ERR_CUDA", -5: "MHC_ERR_DEVICE_TIMEOUT"}
+SCHEDULES = {"auto": 0, "split": 1}
+
+
+class MhcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = lib().mhc_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({detail})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded C library (ctypes).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise ImportError(f"libmhc.so not built at {path}; run manifold_constrained_hyper_mhc_gb300._build.build()")
+            L = ctypes.CDLL(path)
+            P, I64, F, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+            L.mhc_workspace_size.argtypes = [I64, I64]
+            L.mhc_workspace_size.restype = Z
+            L.mhc_shifted_post_pre.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
+                                               P, P, P, P, P, P, Z, P]
+            L.mhc_shifted_post_pre.restype = I
+            L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
+            L.mhc_post.restype = I
+            L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
+            L.mhc_pre.restype = I
+            L.mhc_set_schedule.argtypes = [I]
+            L.mhc_set_schedule.restype = I
+            L.mhc_auto_schedule.argtypes = [I64, I64]
+            L.mhc_auto_schedule.restype = I
+            L.mhc_check_status.argtypes = [P, P]
+            L.mhc_check_status.restype = I
+            L.mhc_status_string.argtypes = [I]
+            L.mhc_status_string.restype = ctypes.c_char_p
+            L.mhc_last_launch_count.argtypes = []
+            L.mhc_last_launch_count.restype = I
+            L.mhc_last_error.argtypes = []
+            L.mhc_last_error.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc, where):
+    if rc != OK:
+        raise MhcError(rc, where)
+
+
+def workspace_size(T: int, H: int) -> int:
+    return int(lib().mhc_workspace_size(int(T), int(H)))
+
+
+def new_workspace(T: int, H: int, device=None):
+    """A zero-filled workspace (uint8 tensor) for calls with up to T tokens of size H."""
+    torch = _torch()
+    return torch.zeros(max(workspace_size(T, H), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _bf16(t, name, shape):
+    torch = _torch()
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bfloat16 (or its 16-bit bit pattern), got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+def _f32(t, name, shape):
+    torch = _torch()
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+def _outputs(T, H, device, out, with_residual):
+    torch = _torch()
+    out = dict(out or {})
+    if with_residual:
+        out.setdefault("residual_out", torch.empty((T, 4, H), dtype=torch.bfloat16, device=device))
+    out.setdefault("layer_in", torch.empty((T, H), dtype=torch.bfloat16, device=device))
+    out.setdefault("pre_mix", torch.empty((T, 4), dtype=torch.float32, device=device))
+    out.setdefault("post_mix", torch.empty((T, 4), dtype=torch.float32, device=device))
+    out.setdefault("comb_res_mix", torch.empty((T, 4, 4), dtype=torch.float32, device=device))
+    return out
+
+
+def shifted_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                     rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                     sinkhorn_iters=20, out=None, workspace=None, stream=None):
+    """mhc_shifted_post_pre: the fused post+pre step.  Returns a dict with
+    residual_out [T,4,H] bf16, layer_in [T,H] bf16, pre_mix [T,4], post_mix [T,4],
+    comb_res_mix [T,4,4] (fp32).  ``out`` may supply preallocated outputs."""
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
+    _bf16(rmsnorm_weight, "rmsnorm_weight", (H,))
+    dev = residual.device
+    o = _outputs(T, H, dev, out, True)
+    ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    rc = lib().mhc_shifted_post_pre(
+        _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
+        _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
+        hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
+        _ptr(o["pre_mix"]), _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream, dev))
+    _check(rc, "mhc_shifted_post_pre")
+    return o
+
+
+def post(residual, layer_out, prev_post_mix, prev_comb_res_mix, *, out=None, stream=None):
+    """mhc_post: step (1) only.  Returns residual_out [T,4,H] bf16."""
+    torch = _torch()
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    o = out if out is not None else torch.empty((T, 4, H), dtype=torch.bfloat16, device=residual.device)
+    rc = lib().mhc_post(_ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix),
+                        T, H, _ptr(o), _stream(stream, residual.device))
+    _check(rc, "mhc_post")
+    return o
+
+
+def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,
+        sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None):
+    """mhc_pre: steps (2)-(4) from post-updated streams.  Returns the fused call's
+    outputs without residual_out."""
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H))
+    _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
+    _bf16(rmsnorm_weight, "rmsnorm_weight", (H,))
+    dev = residual.device
+    o = _outputs(T, H, dev, out, False)
+    ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    rc = lib().mhc_pre(_ptr(residual), _ptr(phi), _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight),
+                       T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, int(sinkhorn_iters),
+                       _ptr(o["layer_in"]), _ptr(o["pre_mix"]), _ptr(o["post_mix"]),
+                       _ptr(o["comb_res_mix"]), _ptr(ws), ws.numel() * ws.element_size(),
+                       _stream(stream, dev))
+    _check(rc, "mhc_pre")
+    return o
+
+
+def set_schedule(name_or_id):
+    sid = SCHEDULES[name_or_id] if isinstance(name_or_id, str) else int(name_or_id)
+    _check(lib().mhc_set_schedule(sid), "mhc_set_schedule")
+
+
+def auto_schedule(T: int, H: int) -> int:
+    return int(lib().mhc_auto_schedule(int(T), int(H)))
+
+
+def last_launch_count() -> int:
+    """Kernels launched by the last library call on this thread."""
+    return int(lib().mhc_last_launch_count())
+
+
+def check_status(workspace, stream=None):
+    """Synchronises the stream and raises MhcError if a device-side wait timed out."""
+    _check(lib().mhc_check_status(_ptr(workspace), _stream(stream, workspace.device)), "mhc_check_status")

@@ -1,0 +1,299 @@
+// C-ABI layer of libmhc.so: argument validation, schedule choice, launches.
+// The contract of every entry point is stated in include/mhc.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "mhc.h"
+#include "mhc_kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local int g_launches = 0;
+std::atomic<int> g_forced_schedule{MHC_SCHEDULE_AUTO};
+
+mhc_status fail(mhc_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+mhc_status fail(mhc_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+mhc_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(MHC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+mhc_status check_sizes(int64_t T, int64_t H) {
+    if (T < 0 || T > MHC_MAX_TOKENS)
+        return fail(MHC_ERR_INVALID_ARG, "T=%lld outside [0, %d]", (long long)T, MHC_MAX_TOKENS);
+    if (H < 8 || H > MHC_MAX_HIDDEN || H % 8 != 0)
+        return fail(MHC_ERR_INVALID_ARG, "H=%lld must be a multiple of 8 in [8, %d]", (long long)H,
+                    MHC_MAX_HIDDEN);
+    return MHC_OK;
+}
+
+mhc_status check_ptrs(std::initializer_list<std::pair<const void *, const char *>> ptrs) {
+    for (auto &pn : ptrs) {
+        if (pn.first == nullptr) return fail(MHC_ERR_INVALID_ARG, "%s is NULL", pn.second);
+        if (!aligned16(pn.first)) return fail(MHC_ERR_INVALID_ARG, "%s is not 16-byte aligned", pn.second);
+    }
+    return MHC_OK;
+}
+
+mhc_status check_scalars(float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                         float sinkhorn_eps, int iters) {
+    auto bad_eps = [](float e) { return !std::isfinite(e) || e < 0.f; };
+    if (bad_eps(hc_norm_eps)) return fail(MHC_ERR_INVALID_ARG, "hc_norm_eps must be finite and >= 0");
+    if (bad_eps(rmsnorm_eps)) return fail(MHC_ERR_INVALID_ARG, "rmsnorm_eps must be finite and >= 0");
+    if (bad_eps(sinkhorn_eps)) return fail(MHC_ERR_INVALID_ARG, "sinkhorn_eps must be finite and >= 0");
+    if (!std::isfinite(hc_post_scale)) return fail(MHC_ERR_INVALID_ARG, "hc_post_scale must be finite");
+    if (iters < 0 || iters > MHC_MAX_SINKHORN_ITERS)
+        return fail(MHC_ERR_INVALID_ARG, "sinkhorn_iters=%d outside [0, %d]", iters, MHC_MAX_SINKHORN_ITERS);
+    return MHC_OK;
+}
+
+struct Device {
+    int id, sms, major, minor;
+};
+
+mhc_status current_device(Device &d) {
+    cudaError_t e = cudaGetDevice(&d.id);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, d.id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, d.id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, d.id)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (d.major != 10 || d.minor != 3)
+        return fail(MHC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                    d.id, d.major, d.minor);
+    return MHC_OK;
+}
+
+size_t workspace_bytes_for(int64_t T, int64_t H) {
+    size_t b = mhc::kControlBytes + mhc::split_workspace_bytes(T, H);
+    return (b + 255) & ~size_t(255);
+}
+
+int choose_schedule(int64_t /*T*/, int64_t /*H*/) {
+    const int forced = g_forced_schedule.load(std::memory_order_relaxed);
+    if (forced != MHC_SCHEDULE_AUTO) return forced;
+    return MHC_SCHEDULE_SPLIT;
+}
+
+// Common body of the fused call (post != nullptr) and the pre-only call.
+mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                        const float *prev_post_mix, const float *prev_comb_res_mix,
+                        const float *phi, const float *bias, const float *mix_scales,
+                        const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps,
+                        float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps,
+                        int sinkhorn_iters, mhc_bf16 *residual_out, mhc_bf16 *layer_in_out,
+                        float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+                        void *workspace, size_t workspace_bytes, void *stream, bool fused) {
+    mhc_status st;
+    g_launches = 0;
+    if ((st = check_sizes(T, H)) != MHC_OK) return st;
+    if ((st = check_scalars(hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters)) != MHC_OK)
+        return st;
+    if (T == 0) return MHC_OK;
+    if ((st = check_ptrs({{residual, "residual"}, {phi, "phi"}, {bias, "bias"},
+                          {mix_scales, "mix_scales"}, {rmsnorm_weight, "rmsnorm_weight"},
+                          {layer_in_out, "layer_in_out"}, {pre_mix_out, "pre_mix_out"},
+                          {post_mix_out, "post_mix_out"}, {comb_res_mix_out, "comb_res_mix_out"}})) != MHC_OK)
+        return st;
+    if (fused && (st = check_ptrs({{layer_out, "layer_out"}, {prev_post_mix, "prev_post_mix"},
+                                   {prev_comb_res_mix, "prev_comb_res_mix"},
+                                   {residual_out, "residual_out"}})) != MHC_OK)
+        return st;
+    if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(MHC_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    const size_t need = workspace_bytes_for(T, H);
+    if (workspace_bytes < need)
+        return fail(MHC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+
+    const size_t tok = (size_t)T;
+    const Span sR{residual, tok * 4 * H * 2}, sY{fused ? layer_out : nullptr, tok * H * 2},
+        sPP{fused ? prev_post_mix : nullptr, tok * 16}, sPC{fused ? prev_comb_res_mix : nullptr, tok * 64},
+        sPhi{phi, (size_t)H * 4 * 24 * 4}, sB{bias, 96}, sMS{mix_scales, 12}, sG{rmsnorm_weight, (size_t)H * 2},
+        sW{workspace, need};
+    const Span ins[] = {sR, sY, sPP, sPC, sPhi, sB, sMS, sG};
+    const Span oRo{fused ? residual_out : nullptr, tok * 4 * H * 2}, oX{layer_in_out, tok * H * 2},
+        oPre{pre_mix_out, tok * 16}, oPost{post_mix_out, tok * 16}, oRes{comb_res_mix_out, tok * 64};
+    const Span outs[] = {oRo, oX, oPre, oPost, oRes, sW};
+    const char *out_names[] = {"residual_out", "layer_in_out", "pre_mix_out", "post_mix_out",
+                               "comb_res_mix_out", "workspace"};
+    for (int o = 0; o < 6; ++o) {
+        for (int i = 0; i < 8; ++i) {
+            if (o == 0 && i == 0 && residual_out == residual) continue;  // in-place residual update
+            if (overlap(outs[o], ins[i]))
+                return fail(MHC_ERR_INVALID_ARG, "%s overlaps an input", out_names[o]);
+        }
+        for (int p = o + 1; p < 6; ++p)
+            if (overlap(outs[o], outs[p]))
+                return fail(MHC_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], out_names[p]);
+    }
+
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
+
+    // mix_scales stays a device pointer: the kernels read the three alphas.
+    mhc::Scalars s{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
+    const int sched = choose_schedule(T, H);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    switch (sched) {
+        case MHC_SCHEDULE_SPLIT: {
+            mhc::SplitArgs a{};
+            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
+            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+            a.T = T; a.H = (int)H; a.s = s;
+            a.R_out = fused ? residual_out : nullptr;
+            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.res_out = comb_res_mix_out;
+            a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            e = mhc::launch_split(a, cs);
+            g_launches = 3;
+            break;
+        }
+        default:
+            return fail(MHC_ERR_UNSUPPORTED, "schedule %d is not available", sched);
+    }
+    if (e != cudaSuccess) {
+        g_launches = 0;
+        return cuda_fail(e, "kernel launch");
+    }
+    return MHC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mhc_workspace_size(int64_t T, int64_t H) {
+    if (T < 0 || H < 0) return 0;
+    return workspace_bytes_for(T, H);
+}
+
+mhc_status mhc_shifted_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                                const float *prev_post_mix, const float *prev_comb_res_mix,
+                                const float *phi, const float *bias, const float *mix_scales,
+                                const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
+                                float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                                float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+                                mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                                float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                        comb_res_mix_out, workspace, workspace_bytes, stream, true);
+}
+
+mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const float *bias,
+                   const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
+                   float hc_norm_eps, float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps,
+                   int sinkhorn_iters, mhc_bf16 *layer_in_out, float *pre_mix_out,
+                   float *post_mix_out, float *comb_res_mix_out, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    return run_post_pre(residual, nullptr, nullptr, nullptr, phi, bias, mix_scales, rmsnorm_weight, T,
+                        H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters,
+                        nullptr, layer_in_out, pre_mix_out, post_mix_out, comb_res_mix_out, workspace,
+                        workspace_bytes, stream, false);
+}
+
+mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+                    const float *prev_comb_res_mix, int64_t T, int64_t H, mhc_bf16 *residual_out,
+                    void *stream) {
+    mhc_status st;
+    g_launches = 0;
+    if ((st = check_sizes(T, H)) != MHC_OK) return st;
+    if (T == 0) return MHC_OK;
+    if ((st = check_ptrs({{residual, "residual"}, {layer_out, "layer_out"}, {prev_post_mix, "prev_post_mix"},
+                          {prev_comb_res_mix, "prev_comb_res_mix"}, {residual_out, "residual_out"}})) != MHC_OK)
+        return st;
+    const size_t tok = (size_t)T;
+    const Span o{residual_out, tok * 4 * H * 2};
+    if (residual_out != residual && overlap(o, {residual, tok * 4 * H * 2}))
+        return fail(MHC_ERR_INVALID_ARG, "residual_out overlaps residual");
+    if (overlap(o, {layer_out, tok * H * 2}) || overlap(o, {prev_post_mix, tok * 16}) ||
+        overlap(o, {prev_comb_res_mix, tok * 64}))
+        return fail(MHC_ERR_INVALID_ARG, "residual_out overlaps an input");
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
+    cudaError_t e = mhc::launch_post(residual, layer_out, prev_post_mix, prev_comb_res_mix, T, (int)H,
+                                     residual_out, dev.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches = 1;
+    return MHC_OK;
+}
+
+mhc_status mhc_set_schedule(int schedule) {
+    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT)
+        return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+    g_forced_schedule.store(schedule, std::memory_order_relaxed);
+    return MHC_OK;
+}
+
+int mhc_auto_schedule(int64_t T, int64_t H) {
+    (void)T;
+    (void)H;
+    return MHC_SCHEDULE_SPLIT;
+}
+
+mhc_status mhc_check_status(void *workspace, void *stream) {
+    if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    if (word != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status clear)");
+        return fail(MHC_ERR_DEVICE_TIMEOUT, "device status word 0x%08x", word);
+    }
+    return MHC_OK;
+}
+
+const char *mhc_status_string(int status) {
+    switch (status) {
+        case MHC_OK: return "MHC_OK: success";
+        case MHC_ERR_INVALID_ARG: return "MHC_ERR_INVALID_ARG: invalid argument";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: unsupported device or schedule";
+        case MHC_ERR_WORKSPACE: return "MHC_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case MHC_ERR_CUDA: return "MHC_ERR_CUDA: CUDA runtime error";
+        case MHC_ERR_DEVICE_TIMEOUT: return "MHC_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+        default: return "unknown mhc_status";
+    }
+}
+
+const char *mhc_last_error(void) { return g_last_error.c_str(); }
+
+int mhc_last_launch_count(void) { return g_launches; }
+
+}  // extern "C"

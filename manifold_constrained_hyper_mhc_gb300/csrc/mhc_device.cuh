@@ -1,0 +1,148 @@
+// Device-side building blocks shared by every schedule of the mHC post+pre
+// kernels.  Each schedule computes the same fp32 expressions in the same order
+// through these helpers, so the post (residual update) and the combine are bit
+// for bit the same whichever schedule runs them.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace mhc {
+
+constexpr int kHC = 4;      // hc_mult: residual streams per token
+constexpr int kNumMix = 24; // 4 pre + 4 post + 16 residual-mix logits
+constexpr int kVec = 8;     // bf16 elements per 16-byte vector
+
+struct Scalars {
+    float hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps;
+    int sinkhorn_iters;
+};
+
+// ---- 16-byte vector access ------------------------------------------------
+
+// Streaming load of data that is read once (evict-first in L1/L2).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+// Load through the read-only path (data reused across CTAs, e.g. weights).
+__device__ __forceinline__ uint4 ld_ro(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, uint4 v) {
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(w[q] << 16);
+        f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 pack8_rn(const float (&f)[8]) {
+    return make_uint4(pack2_rn(f[0], f[1]), pack2_rn(f[2], f[3]), pack2_rn(f[4], f[5]),
+                      pack2_rn(f[6], f[7]));
+}
+
+// ---- step (1): post --------------------------------------------------------
+// R'[i][h] = post[i] * Y[h] + sum_{j=0..3} comb[j][i] * R[j][h], fp32 fma chain
+// in this order, then round to nearest even bf16.  out[i] is the rounded
+// stream i as bf16 bits; rf[i][e] the rounded values widened back to fp32.
+__device__ __forceinline__ void post_vec8(const uint4 (&r)[kHC], uint4 y, const float *comb /*[4][4]*/,
+                                          const float *post /*[4]*/, uint4 (&out)[kHC],
+                                          float (&rf)[kHC][8]) {
+    float R[kHC][8], Y[8];
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) unpack8(r[j], R[j]);
+    unpack8(y, Y);
+#pragma unroll
+    for (int i = 0; i < kHC; ++i) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = post[i] * Y[e];
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) {
+            const float c = comb[j * kHC + i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(c, R[j][e], acc[e]);
+        }
+        out[i] = pack8_rn(acc);
+        unpack8(out[i], rf[i]);
+    }
+}
+
+// ---- step (4): combine ------------------------------------------------------
+// X[h] = sum_i pre[i] * R'[i][h], fp32: pre0*R0, then fma with i = 1, 2, 3.
+__device__ __forceinline__ void combine_vec8(const float (&rf)[kHC][8], const float (&pre)[kHC],
+                                             float (&x)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float a = pre[0] * rf[0][e];
+        a = fmaf(pre[1], rf[1][e], a);
+        a = fmaf(pre[2], rf[2][e], a);
+        a = fmaf(pre[3], rf[3][e], a);
+        x[e] = a;
+    }
+}
+
+// out[h] = bf16((X[h] * rstd) * gamma[h])
+__device__ __forceinline__ uint4 norm_vec8(const float (&x)[8], float rstd, uint4 g) {
+    float G[8], o[8];
+    unpack8(g, G);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = (x[e] * rstd) * G[e];
+    return pack8_rn(o);
+}
+
+// ---- step (3): heads and Sinkhorn, one warp per token -----------------------
+// Input: every lane holds the finished logit z[lane] for lanes 0..23 (the
+// others ignored).  Lanes 0-3 produce pre, 4-7 post, 8-23 the residual mix
+// entry e = lane - 8 (row a = e / 4, column c = e % 4).  Row and column sums
+// are taken in the fixed order ((m0 + m1) + (m2 + m3)).
+// mix_scales = (alpha_pre, alpha_post, alpha_res), a device pointer.
+__device__ __forceinline__ float heads_and_sinkhorn(float z, const float *bias,
+                                                    const float *mix_scales, const Scalars &s) {
+    const int lane = threadIdx.x & 31;
+    float v = 0.f;
+    if (lane < 4) {
+        v = 1.f / (1.f + expf(-(mix_scales[0] * z + bias[lane])));
+    } else if (lane < 8) {
+        v = s.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
+    } else if (lane < 24) {
+        v = expf(mix_scales[2] * z + bias[lane]);
+    }
+    const int e = (lane - 8) & 15;
+    const int a = e >> 2, c = e & 3;
+    const int rbase = 8 + 4 * a, cbase = 8 + c;
+    for (int it = 0; it < s.sinkhorn_iters; ++it) {
+        float m0 = __shfl_sync(0xffffffffu, v, rbase + 0);
+        float m1 = __shfl_sync(0xffffffffu, v, rbase + 1);
+        float m2 = __shfl_sync(0xffffffffu, v, rbase + 2);
+        float m3 = __shfl_sync(0xffffffffu, v, rbase + 3);
+        float rs = (m0 + m1) + (m2 + m3);
+        if (lane >= 8 && lane < 24) v = v / (rs + s.sinkhorn_eps);
+        m0 = __shfl_sync(0xffffffffu, v, cbase + 0);
+        m1 = __shfl_sync(0xffffffffu, v, cbase + 4);
+        m2 = __shfl_sync(0xffffffffu, v, cbase + 8);
+        m3 = __shfl_sync(0xffffffffu, v, cbase + 12);
+        float cs = (m0 + m1) + (m2 + m3);
+        if (lane >= 8 && lane < 24) v = v / (cs + s.sinkhorn_eps);
+    }
+    return v;
+}
+
+// Deterministic warp sum (fixed xor-tree order).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace mhc

@@ -1,0 +1,45 @@
+// Internal launch interface between the C-ABI layer (mhc_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mhc_device.cuh"
+
+namespace mhc {
+
+// Split schedule geometry (also sizes its workspace).
+constexpr int kSplitTok = 16;    // tokens per CTA of the partial-sum kernel
+constexpr int kSplitH = 256;     // hidden elements per chunk
+constexpr int kPartStride = 32;  // floats per (token, chunk) record: z[24], square sum, pad
+
+// Bytes at the start of every workspace reserved for the control block
+// (device status word, barrier counters).
+constexpr size_t kControlBytes = 256;
+
+struct SplitArgs {
+    const uint16_t *R;  // residual (fused) or already post-updated residual (pre only)
+    const uint16_t *Y;
+    const float *prev_post, *prev_comb, *phi, *bias, *mix_scales;
+    const uint16_t *gamma;
+    int64_t T;
+    int H;
+    Scalars s;
+    uint16_t *R_out;  // nullptr: pre only (R already holds R')
+    uint16_t *X_out;
+    float *pre_out, *post_out, *res_out;
+    float *part;  // workspace: [T][ceil(H/256)][32] floats
+};
+
+inline size_t split_workspace_bytes(int64_t T, int64_t H) {
+    const int64_t nchunk = (H + kSplitH - 1) / kSplitH;
+    return (size_t)T * (size_t)nchunk * kPartStride * sizeof(float);
+}
+
+cudaError_t launch_split(const SplitArgs &a, cudaStream_t stream);
+cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
+                        const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
+                        cudaStream_t stream);
+
+}  // namespace mhc

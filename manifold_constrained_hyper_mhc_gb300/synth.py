@@ -27,7 +27,9 @@ its own (sampled parity checks at full size need this).
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import itertools
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -78,9 +80,11 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
     Random draws are finite, so no NaN handling is needed here.
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    u = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
-    return (u >> np.uint32(16)).astype(np.uint16)
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    u += (u >> np.uint32(16)) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u >>= np.uint32(16)
+    return u.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -147,15 +151,19 @@ def tokens(w: Workload, t0: int = 0, t1: int | None = None):
     Y = np.empty((n, w.H), np.uint16)
     post = np.empty((n, HC), np.float32)
     comb = np.empty((n, HC, HC), np.float32)
-    b = t0 // BLOCK
-    while b * BLOCK < t1:
+
+    def fill(b):
         Rb, Yb, pb, cb = _block(w, b)
         lo = max(t0, b * BLOCK)
         hi = min(t1, b * BLOCK + len(Yb))
         s = slice(lo - b * BLOCK, hi - b * BLOCK)
         d = slice(lo - t0, hi - t0)
         R[d], Y[d], post[d], comb[d] = Rb[s], Yb[s], pb[s], cb[s]
-        b += 1
+
+    blocks = range(t0 // BLOCK, (t1 + BLOCK - 1) // BLOCK) if n else range(0)
+    # numpy's generators release the GIL while filling, so blocks run in parallel
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(blocks), os.cpu_count() or 1))) as ex:
+        list(ex.map(fill, blocks))
     return R, Y, post, comb
 
 
