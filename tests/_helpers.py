@@ -3,14 +3,19 @@ the same seeded inputs.
 
 Tolerances (derived from the arithmetic, and the bar the op is held to):
   * bf16 outputs pass per element when |gpu - oracle| <= 2 bf16 ulp of the
-    oracle value, or <= 1e-2 * |oracle|, or <= an absolute floor that bounds
-    the fp32 accumulation error of that element:
+    oracle value, or <= 1e-2 * |oracle|, or <= floor + 1 ulp, where the floor
+    bounds the error of that element before its final bf16 rounding (which can
+    add one more ulp):
       - R'     : floor = 2^-19 * (sum_j |comb[j][i] R[j][h]| + |post[i] Y[h]|)
                  (five fp32 roundings are at most ~5 * 2^-24 of that sum)
-      - layer_in: floor = 2^-16 * rstd * |gamma[h]| * sum_i |pre[i] R'[i][h]|
-                 (the fp32 combine, the fp32 square sum over H and the fp32
-                 mixes each contribute at most ~1e-6 relative to that scale)
-    The floor only matters where the result cancels to far below its terms.
+      - layer_in: floor = rstd * |gamma[h]| * sum_i |pre[i]| (ulp(R'[i][h]) + 2^-16 |R'[i][h]|)
+                 The first term carries over the allowed 1-ulp difference of the
+                 bf16 R' (the GPU rounds an fp32 sum, the oracle an fp64 one, so
+                 an element on a rounding boundary may land on either side)
+                 into X = sum_i pre[i] R'[i]; the second bounds the fp32
+                 combine, the fp32 square sum over H and the fp32 mixes (each at
+                 most ~1e-6 relative to that scale).
+    The floor only matters where X is smaller than its terms.
   * fp32 mixes (pre, post, comb_res_mix) pass when |gpu - oracle| <= 1e-4.
 """
 from __future__ import annotations
@@ -38,7 +43,7 @@ def bf16_check(got_bits, want_bits, floor):
     d = np.abs(g - w)
     u = ulp_bf16(w)
     rel_ok = (d <= 2 * u) | (d <= 1e-2 * np.abs(w))
-    ok = rel_ok | (d <= floor)
+    ok = rel_ok | (d <= floor + u)
     return int((~ok).sum()), float((d / u).max()) if d.size else 0.0, int((ok & ~rel_ok).sum())
 
 
@@ -52,8 +57,8 @@ def residual_floor(R_bits, Y_bits, prev_post, prev_comb):
 
 def layer_in_floor(Rp_bits, pre, rstd, gamma_bits):
     Rp = np.abs(F(Rp_bits).astype(np.float64))
-    S = np.einsum("ni,nih->nh", np.abs(pre), Rp)
-    return 2.0 ** -16 * rstd[:, None] * np.abs(F(gamma_bits).astype(np.float64))[None, :] * S
+    S = np.einsum("ni,nih->nh", np.abs(pre), ulp_bf16(Rp) + 2.0 ** -16 * Rp)
+    return rstd[:, None] * np.abs(F(gamma_bits).astype(np.float64))[None, :] * S
 
 
 def compare_fused(gpu: dict, ref: dict, inputs, gamma, t0=0, label=""):
