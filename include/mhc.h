@@ -121,6 +121,33 @@ MHC_API mhc_status mhc_shifted_post_pre(
     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/* The fused step (1)-(4) for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.
+ * Some callers cannot call cudaMalloc where they run the op: a host framework
+ * that owns all device memory and only hands out the tensors it manages, a
+ * plugin that must not grow the process's memory footprint, or a hot path where
+ * an allocation would synchronise the device.  Such a caller passes inputs and
+ * outputs only (arguments and outputs as in mhc_shifted_post_pre, no workspace);
+ * the scratch the kernels need is a 4 MiB static device array inside this
+ * library, which every GPU that loads the library holds until the process exits.
+ *   - Limit: mhc_workspace_size(T, H) must be at most 4 MiB (at H = 7168 up to
+ *     1170 tokens); larger calls return MHC_ERR_INVALID_ARG and launch nothing,
+ *     with the reason in mhc_last_error().
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; nothing in it needs clearing between calls.  Calls that
+ *     overlap on the GPU (different streams without ordering) race on it.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+MHC_API mhc_status mhc_shifted_post_pre_noalloc(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,
+    const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps,
+    float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+    void *stream);
+
 /* Step (1) alone: the mHC post ("[SM80] Backport mHC fused post + int8
  * all-reduce", "What this fixes").  Needs no workspace. */
 MHC_API mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out,

@@ -190,6 +190,10 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
 
 }  // namespace
 
+namespace mhc {
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace mhc
+
 extern "C" {
 
 size_t mhc_workspace_size(int64_t T, int64_t H) {
