@@ -140,9 +140,9 @@ def run_reference(args, rank, world, dist):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     if rank != 0:
         return
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     phi, bias, ms, gamma = synth.weights(w)
-    n = 512
+    n = min(512, w.T)
     times = []
     for s in range(args.warmup + args.steps):
         tps, nt, el, done = time_oracle(w, phi, bias, ms, gamma, n, 0.0, t_offset=s * n)
@@ -150,12 +150,12 @@ def run_reference(args, rank, world, dist):
             times.append(el)
     ms_step = 1e3 * float(np.mean(times))
     value = n / (ms_step / 1e3)
-    sample = f"{n} consecutive tokens of the {WORKLOAD} workload (T={w.T}, H={w.H}) per step"
+    sample = f"{n} consecutive tokens of the {w.name} workload (T={w.T}, H={w.H}) per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} T={w.T} H={w.H} hc_mult=4", "T": w.T, "H": w.H,
+        "config": {"workload": f"{w.name} T={w.T} H={w.H} hc_mult=4", "T": w.T, "H": w.H,
                    "tokens_per_step": n},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
                          "machine": platform.machine()},
@@ -173,8 +173,10 @@ def run_ours(args, rank, world, lr, dist):
         raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
     dev = torch.device("cuda", lr if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.workload]
     T, H = w.T, w.H
+    if args.schedule != "auto":
+        mhc.set_schedule(args.schedule)
     phi, bias, msc, gamma = synth.weights(w)
     R, Y, pp, pc = synth.tokens(w)
 
@@ -266,12 +268,13 @@ def run_ours(args, rank, world, lr, dist):
     peak, peak_src = peaks()
     abytes = algorithmic_bytes(T, H)
     achieved = abytes / (ms_step / 1e3) / 1e9
-    sched = {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
+    sched = args.schedule if args.schedule != "auto" else \
+        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} T={T} H={H} hc_mult=4", "T": T, "H": H, "io": "bf16 streams, fp32 mixes",
+        "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H, "io": "bf16 streams, fp32 mixes",
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
                    "hbm_gbs": achieved, "hbm_frac": achieved / peak},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -283,9 +286,9 @@ def run_ours(args, rank, world, lr, dist):
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        tps, nt, el, done = time_oracle(w, phi, bias, msc, gamma, 1024, 10.0)
+        tps, nt, el, done = time_oracle(w, phi, bias, msc, gamma, min(1024, T), 10.0)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": nt, "kind": "oracle",
-                                "sample": f"first 1024 tokens of {WORKLOAD} (T={T}, H={H}), repeated for "
+                                "sample": f"first {min(1024, T)} tokens of {w.name} (T={T}, H={H}), repeated for "
                                           f"{el:.1f} s ({done} tokens)", "machine": platform.machine()}
     print(json.dumps(line), flush=True)
 
@@ -297,6 +300,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster"])
     args = ap.parse_args()
     rank, world, lr, dist = dist_setup()
     try:

@@ -89,7 +89,8 @@ typedef enum mhc_status {
 /* Kernel schedules.  AUTO picks by T, H and the SM count. */
 typedef enum mhc_schedule {
     MHC_SCHEDULE_AUTO = 0,
-    MHC_SCHEDULE_SPLIT = 1   /* three launches: post + partial sums, mixes, combine + RMSNorm */
+    MHC_SCHEDULE_SPLIT = 1,  /* three launches: post + partial sums, mixes, combine + RMSNorm */
+    MHC_SCHEDULE_CLUSTER = 2 /* one pass over HBM: thread-block clusters split the hidden dim */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -2,6 +2,7 @@
 // The contract of every entry point is stated in include/mhc.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cmath>
@@ -92,15 +93,30 @@ mhc_status current_device(Device &d) {
     return MHC_OK;
 }
 
+// Cluster schedule geometry: cluster size and tokens per group.
+constexpr int kClusterC = 8;
+constexpr int kClusterG = 16;
+constexpr size_t kMaxDynSmem = 227 * 1024;
+
+bool cluster_fits(int64_t H) {
+    return mhc::fused_smem_bytes((int)H, kClusterC, kClusterG) <= kMaxDynSmem;
+}
+
 size_t workspace_bytes_for(int64_t T, int64_t H) {
-    size_t b = mhc::kControlBytes + mhc::split_workspace_bytes(T, H);
+    size_t sched = mhc::split_workspace_bytes(T, H);
+    if (H >= 8 && H <= MHC_MAX_HIDDEN) sched = std::max(sched, mhc::fused_pack_bytes((int)H, kClusterC));
+    size_t b = mhc::kControlBytes + sched;
     return (b + 255) & ~size_t(255);
 }
 
-int choose_schedule(int64_t /*T*/, int64_t /*H*/) {
+int auto_schedule(int64_t /*T*/, int64_t H) {
+    return cluster_fits(H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
+}
+
+int choose_schedule(int64_t T, int64_t H) {
     const int forced = g_forced_schedule.load(std::memory_order_relaxed);
     if (forced != MHC_SCHEDULE_AUTO) return forced;
-    return MHC_SCHEDULE_SPLIT;
+    return auto_schedule(T, H);
 }
 
 // Common body of the fused call (post != nullptr) and the pre-only call.
@@ -176,6 +192,23 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
             e = mhc::launch_split(a, cs);
             g_launches = 3;
+            break;
+        }
+        case MHC_SCHEDULE_CLUSTER: {
+            if (!cluster_fits(H))
+                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster schedule's shared memory",
+                            (long long)H);
+            mhc::FusedArgs a{};
+            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
+            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+            a.T = T; a.H = (int)H; a.s = s;
+            a.R_out = fused ? residual_out : nullptr;
+            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.res_out = comb_res_mix_out;
+            a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            a.C = kClusterC; a.G = kClusterG;
+            e = mhc::launch_fused(a, cs);
+            g_launches = 2;
             break;
         }
         default:
@@ -255,17 +288,13 @@ mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const f
 }
 
 mhc_status mhc_set_schedule(int schedule) {
-    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT)
+    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);
     return MHC_OK;
 }
 
-int mhc_auto_schedule(int64_t T, int64_t H) {
-    (void)T;
-    (void)H;
-    return MHC_SCHEDULE_SPLIT;
-}
+int mhc_auto_schedule(int64_t T, int64_t H) { return auto_schedule(T, H); }
 
 mhc_status mhc_check_status(void *workspace, void *stream) {
     if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");

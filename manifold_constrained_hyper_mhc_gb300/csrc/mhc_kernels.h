@@ -38,6 +38,27 @@ inline size_t split_workspace_bytes(int64_t T, int64_t H) {
 }
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t stream);
+
+// Cluster schedule (kernels_fused.cu).
+struct FusedArgs {
+    const uint16_t *R;  // residual (fused) or already post-updated residual (pre only)
+    const uint16_t *Y;
+    const float *prev_post, *prev_comb, *phi, *bias, *mix_scales;
+    const uint16_t *gamma;
+    int64_t T;
+    int H;
+    Scalars s;
+    uint16_t *R_out;  // nullptr: pre only
+    uint16_t *X_out;
+    float *pre_out, *post_out, *res_out;
+    uint4 *phi_pack;  // workspace: fused_pack_bytes(H, C)
+    int C, G;         // cluster size, tokens per group
+};
+
+int fused_slice(int H, int C);                     // hidden elements per CTA (multiple of 16)
+size_t fused_pack_bytes(int H, int C);             // packed phi fragments
+size_t fused_smem_bytes(int H, int C, int G);      // dynamic shared memory per CTA
+cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
