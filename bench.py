@@ -174,6 +174,8 @@ def run_ours(args, rank, world, lr, dist):
     dev = torch.device("cuda", lr if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        w = synth.Workload(f"{w.name}[:{args.tokens}]", args.tokens, w.H, w.seed, w.token_scale, w.special_tokens)
     T, H = w.T, w.H
     if args.schedule != "auto":
         mhc.set_schedule(args.schedule)
@@ -301,7 +303,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16"])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     args = ap.parse_args()
     rank, world, lr, dist = dist_setup()
     try:

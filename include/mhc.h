@@ -89,8 +89,12 @@ typedef enum mhc_status {
 /* Kernel schedules.  AUTO picks by T, H and the SM count. */
 typedef enum mhc_schedule {
     MHC_SCHEDULE_AUTO = 0,
-    MHC_SCHEDULE_SPLIT = 1,  /* three launches: post + partial sums, mixes, combine + RMSNorm */
-    MHC_SCHEDULE_CLUSTER = 2 /* one pass over HBM: thread-block clusters split the hidden dim */
+    MHC_SCHEDULE_SPLIT = 1,       /* three launches: post + partial sums, mixes, combine + RMSNorm */
+    MHC_SCHEDULE_CLUSTER = 2,     /* one pass over HBM, clusters split the hidden dim; default geometry */
+    MHC_SCHEDULE_CLUSTER_8x16 = 3,/* clusters of 8 CTAs, 16 tokens per group, 1 CTA per SM */
+    MHC_SCHEDULE_CLUSTER_8x8 = 4, /* clusters of 8 CTAs, 8 tokens per group, 2 CTAs per SM */
+    MHC_SCHEDULE_CLUSTER16 = 5    /* clusters of 16 CTAs, 16 tokens per group, phi resident in
+                                     tensor memory, next group's rows fetched by bulk async copies */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -26,6 +26,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "mhc_device.cuh"
 #include "mhc_kernels.h"
@@ -36,8 +37,10 @@ namespace mhc {
 
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
+
+// Split cluster barrier: arrive (release) now, wait (acquire) later.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,7 +69,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4 &a, uint32_t
 
 // Shared memory of one CTA (dynamic).  R' rows are padded by 16 bytes so the
 // eight rows an ldmatrix reads fall into distinct bank groups.
-template <int G>
+template <int G, int kWarps>
 struct FusedSmem {
     static constexpr int kPartStride = 32;
     // offsets in bytes
@@ -113,8 +116,8 @@ pack_phi_kernel(const float *__restrict__ phi, int H, int C, int Hs, uint4 *__re
     out[idx] = v;
 }
 
-template <int C, int G, bool kPost>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int C, int G, int kWarps, int kMinBlocks, bool kPost>
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks)
 fused_cluster_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y,
                      const float *__restrict__ prev_post, const float *__restrict__ prev_comb,
                      const uint4 *__restrict__ phi_pack, const float *__restrict__ bias,
@@ -122,7 +125,8 @@ fused_cluster_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict_
                      Scalars sc, int64_t T, int H, int Hs, uint16_t *__restrict__ R_out,
                      uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
                      float *__restrict__ post_out, float *__restrict__ res_out) {
-    using SM = FusedSmem<G>;
+    using SM = FusedSmem<G, kWarps>;
+    constexpr int kThreads = kWarps * 32;
     extern __shared__ __align__(16) unsigned char smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int c = (int)cluster.block_rank();
@@ -293,28 +297,39 @@ fused_cluster_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict_
         }
         cluster.sync();  // #1: every CTA's partial records are complete
 
-        // ---- P3: owner CTA of token g (g % C == c) reduces the C records, heads, Sinkhorn
-        for (int g = c + C * warp; g < gv; g += C * kWarps) {
-            float acc = 0.f;
-            if (lane <= kNumMix) {
-#pragma unroll
-                for (int q = 0; q < C; ++q) acc += cluster.map_shared_rank(sPart, q)[g * 32 + lane];
-            }
-            const float ss = __shfl_sync(0xffffffffu, acc, kNumMix);
-            const float r = 1.f / sqrtf(ss / (float)(kHC * H) + sc.hc_norm_eps);
-            const float v = heads_and_sinkhorn(r * acc, bias, mix_scales, sc);
-            const int64_t t = t0 + g;
-            if (lane < 4) {
-                pre_out[t * 4 + lane] = v;
-#pragma unroll
-                for (int q = 0; q < C; ++q) cluster.map_shared_rank(sPre, q)[g * 4 + lane] = v;
-            } else if (lane < 8) {
-                post_out[t * 4 + lane - 4] = v;
-            } else if (lane < 24) {
-                res_out[t * 16 + lane - 8] = v;
+        // ---- P3: owner CTA of token g (g % C == c) reduces the C records and
+        // pushes pre to every CTA; the post head and the Sinkhorn mix follow
+        // after this warp has arrived at the cluster barrier, so they overlap
+        // the other warps' combine instead of delaying it.
+        float zkeep[(G + C * kWarps - 1) / (C * kWarps)];
+        {
+            int u = 0;
+            for (int g = c + C * warp; g < gv; g += C * kWarps, ++u) {
+                float acc = 0.f;
+                if (lane <= kNumMix) {
+                    for (int q = 0; q < C; ++q) acc += cluster.map_shared_rank(sPart, q)[g * 32 + lane];
+                }
+                const float ss = __shfl_sync(0xffffffffu, acc, kNumMix);
+                const float r = 1.f / sqrtf(ss / (float)(kHC * H) + sc.hc_norm_eps);
+                zkeep[u] = r * acc;
+                const float p = pre_head(zkeep[u], bias, mix_scales);
+                if (lane < 4) {
+                    pre_out[(t0 + g) * 4 + lane] = p;
+                    for (int q = 0; q < C; ++q) cluster.map_shared_rank(sPre, q)[g * 4 + lane] = p;
+                }
             }
         }
-        cluster.sync();  // #2: pre of every token is in every CTA
+        cluster_arrive();  // #2: pre of every token is in every CTA
+        {
+            int u = 0;
+            for (int g = c + C * warp; g < gv; g += C * kWarps, ++u) {
+                const float v = post_and_sinkhorn(zkeep[u], bias, mix_scales, sc);
+                const int64_t t = t0 + g;
+                if (lane >= 4 && lane < 8) post_out[t * 4 + lane - 4] = v;
+                else if (lane >= 8 && lane < 24) res_out[t * 16 + lane - 8] = v;
+            }
+        }
+        cluster_wait();
 
         // ---- P4: combine, square sum of X per token
         for (int g = warp; g < gv; g += kWarps) {
@@ -357,12 +372,18 @@ fused_cluster_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict_
     cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
-template <int C, int G>
-cudaError_t launch_fused_cg(const FusedArgs &a, int Hs, cudaStream_t stream) {
-    using SM = FusedSmem<G>;
-    const size_t smem = SM::bytes(Hs);
-    auto kern = a.R_out != nullptr ? fused_cluster_kernel<C, G, true> : fused_cluster_kernel<C, G, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// Per-device, per-kernel launch set-up, done once: the shared-memory attribute
+// (set to the largest size this kernel can need) and the number of clusters
+// that fit on the device at that size.
+struct LaunchSetup {
+    bool ready = false;
+    int max_clusters = 0;
+};
+constexpr int kMaxDevices = 64;
+
+template <typename Kern>
+cudaError_t launch_setup(Kern kern, int C, int threads, size_t smem_max, LaunchSetup &st) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
     if (e != cudaSuccess) return e;
     if (C > 8) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -374,16 +395,53 @@ cudaError_t launch_fused_cg(const FusedArgs &a, int Hs, cudaStream_t stream) {
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem_max;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(C);
+    e = cudaOccupancyMaxActiveClusters(&st.max_clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (st.max_clusters < 1) return cudaErrorInvalidConfiguration;
+    st.ready = true;
+    return cudaSuccess;
+}
+
+std::mutex g_setup_mu;
+
+template <int C, int G, int NW, int MB>
+cudaError_t launch_fused_cg(const FusedArgs &a, int Hs, cudaStream_t stream) {
+    using SM = FusedSmem<G, NW>;
+    const size_t smem = SM::bytes(Hs);
+    const bool post = a.R_out != nullptr;
+    auto kern = post ? fused_cluster_kernel<C, G, NW, MB, true> : fused_cluster_kernel<C, G, NW, MB, false>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    static LaunchSetup setup[kMaxDevices][2];  // one per template instance and device
+    int max_clusters;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        LaunchSetup &st = setup[dev][post ? 1 : 0];
+        if (!st.ready) {
+            // occupancy at the largest shared-memory size this instance may use
+            e = launch_setup(kern, C, NW * 32, MB == 1 ? 227 * 1024 : 227 * 1024 / MB - 1024, st);
+            if (e != cudaSuccess) return e;
+        }
+        max_clusters = st.max_clusters;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(C);
-    int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int64_t ngroups = (a.T + G - 1) / G;
     const int nclusters = (int)std::min<int64_t>(ngroups, max_clusters);
     cfg.gridDim = dim3(nclusters * C);
@@ -394,6 +452,10 @@ cudaError_t launch_fused_cg(const FusedArgs &a, int Hs, cudaStream_t stream) {
 
 }  // namespace
 
+void launch_pack_phi(const float *phi, int H, int C, int Hs, uint4 *out, int64_t total, cudaStream_t stream) {
+    pack_phi_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(phi, H, C, Hs, out);
+}
+
 int fused_slice(int H, int C) { return ((H + 16 * C - 1) / (16 * C)) * 16; }
 
 size_t fused_pack_bytes(int H, int C) {
@@ -403,7 +465,9 @@ size_t fused_pack_bytes(int H, int C) {
 
 size_t fused_smem_bytes(int H, int C, int G) {
     const int Hs = fused_slice(H, C);
-    return G == 16 ? FusedSmem<16>::bytes(Hs) : (size_t)-1;
+    if (C == 8 && G == 16) return FusedSmem<16, 16>::bytes(Hs);
+    if (C == 8 && G == 8) return FusedSmem<8, 8>::bytes(Hs);
+    return (size_t)-1;
 }
 
 cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
@@ -414,7 +478,8 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // 2. the fused pass
-    if (a.C == 8 && a.G == 16) return launch_fused_cg<8, 16>(a, Hs, stream);
+    if (a.C == 8 && a.G == 16) return launch_fused_cg<8, 16, 16, 1>(a, Hs, stream);
+    if (a.C == 8 && a.G == 8) return launch_fused_cg<8, 8, 8, 2>(a, Hs, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -93,24 +93,44 @@ mhc_status current_device(Device &d) {
     return MHC_OK;
 }
 
-// Cluster schedule geometry: cluster size and tokens per group.
-constexpr int kClusterC = 8;
-constexpr int kClusterG = 16;
+// Cluster schedule geometries: cluster size C, tokens per group G, and the
+// shared-memory budget per CTA (one or two CTAs per SM).
+struct ClusterGeom {
+    int C, G;
+    size_t smem_limit;
+};
 constexpr size_t kMaxDynSmem = 227 * 1024;
+constexpr ClusterGeom kGeom8x16{8, 16, kMaxDynSmem};
+constexpr ClusterGeom kGeom8x8{8, 8, kMaxDynSmem / 2 - 1024};
+constexpr ClusterGeom kGeomDefault = kGeom8x8;
 
-bool cluster_fits(int64_t H) {
-    return mhc::fused_smem_bytes((int)H, kClusterC, kClusterG) <= kMaxDynSmem;
+const ClusterGeom *geom_of(int sched) {
+    switch (sched) {
+        case MHC_SCHEDULE_CLUSTER: return &kGeomDefault;
+        case MHC_SCHEDULE_CLUSTER_8x16: return &kGeom8x16;
+        case MHC_SCHEDULE_CLUSTER_8x8: return &kGeom8x8;
+        default: return nullptr;
+    }
+}
+
+bool cluster_fits(const ClusterGeom &g, int64_t H) {
+    return mhc::fused_smem_bytes((int)H, g.C, g.G) <= g.smem_limit;
 }
 
 size_t workspace_bytes_for(int64_t T, int64_t H) {
     size_t sched = mhc::split_workspace_bytes(T, H);
-    if (H >= 8 && H <= MHC_MAX_HIDDEN) sched = std::max(sched, mhc::fused_pack_bytes((int)H, kClusterC));
+    if (H >= 8 && H <= MHC_MAX_HIDDEN)
+    {
+        for (const ClusterGeom *g : {&kGeom8x16, &kGeom8x8})
+            sched = std::max(sched, mhc::fused_pack_bytes((int)H, g->C));
+        sched = std::max(sched, mhc::fused_tmem_pack_bytes((int)H));
+    }
     size_t b = mhc::kControlBytes + sched;
     return (b + 255) & ~size_t(255);
 }
 
 int auto_schedule(int64_t /*T*/, int64_t H) {
-    return cluster_fits(H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
+    return cluster_fits(kGeomDefault, H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
 }
 
 int choose_schedule(int64_t T, int64_t H) {
@@ -194,8 +214,11 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             g_launches = 3;
             break;
         }
-        case MHC_SCHEDULE_CLUSTER: {
-            if (!cluster_fits(H))
+        case MHC_SCHEDULE_CLUSTER:
+        case MHC_SCHEDULE_CLUSTER_8x16:
+        case MHC_SCHEDULE_CLUSTER_8x8: {
+            const ClusterGeom &geom = *geom_of(sched);
+            if (!cluster_fits(geom, H))
                 return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster schedule's shared memory",
                             (long long)H);
             mhc::FusedArgs a{};
@@ -206,8 +229,24 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
             a.res_out = comb_res_mix_out;
             a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
-            a.C = kClusterC; a.G = kClusterG;
+            a.C = geom.C; a.G = geom.G;
             e = mhc::launch_fused(a, cs);
+            g_launches = 2;
+            break;
+        }
+        case MHC_SCHEDULE_CLUSTER16: {
+            if (!mhc::fused_tmem_supported((int)H))
+                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster16 schedule", (long long)H);
+            mhc::FusedArgs a{};
+            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
+            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+            a.T = T; a.H = (int)H; a.s = s;
+            a.R_out = fused ? residual_out : nullptr;
+            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.res_out = comb_res_mix_out;
+            a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            a.C = 16; a.G = 16;
+            e = mhc::launch_fused_tmem(a, static_cast<unsigned int *>(workspace), cs);
             g_launches = 2;
             break;
         }
@@ -288,7 +327,8 @@ mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const f
 }
 
 mhc_status mhc_set_schedule(int schedule) {
-    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER)
+    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER16 &&
+        geom_of(schedule) == nullptr)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);
     return MHC_OK;

@@ -102,40 +102,67 @@ __device__ __forceinline__ uint4 norm_vec8(const float (&x)[8], float rstd, uint
 }
 
 // ---- step (3): heads and Sinkhorn, one warp per token -----------------------
-// Input: every lane holds the finished logit z[lane] for lanes 0..23 (the
-// others ignored).  Lanes 0-3 produce pre, 4-7 post, 8-23 the residual mix
-// entry e = lane - 8 (row a = e / 4, column c = e % 4).  Row and column sums
-// are taken in the fixed order ((m0 + m1) + (m2 + m3)).
-// mix_scales = (alpha_pre, alpha_post, alpha_res), a device pointer.
-__device__ __forceinline__ float heads_and_sinkhorn(float z, const float *bias,
-                                                    const float *mix_scales, const Scalars &s) {
+// Input: lane n holds the finished logit z[n] for n = 0..23 (other lanes are
+// ignored).  pre_head: lanes 0-3 return pre[lane] (the rest 0).
+__device__ __forceinline__ float pre_head(float z, const float *bias, const float *mix_scales) {
     const int lane = threadIdx.x & 31;
-    float v = 0.f;
-    if (lane < 4) {
-        v = 1.f / (1.f + expf(-(mix_scales[0] * z + bias[lane])));
-    } else if (lane < 8) {
-        v = s.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
-    } else if (lane < 24) {
-        v = expf(mix_scales[2] * z + bias[lane]);
+    return lane < 4 ? 1.f / (1.f + expf(-(mix_scales[0] * z + bias[lane]))) : 0.f;
+}
+
+// Hardware reciprocal approximation (rcp.approx.ftz.f32, within 1 ulp).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// post and residual-mix heads.  Lanes 4-7 return post[lane-4]; lanes 8-23
+// return the Sinkhorn-normalised residual mix entry e = lane - 8 (row a = e/4,
+// column c = e%4).  Every lane gathers the 16 logits and runs the iteration on
+// the whole 4x4 matrix in registers (no shuffles inside the loop): each row,
+// then each column, is multiplied by the reciprocal of (sum + sinkhorn_eps);
+// sums are taken in the order ((m0 + m1) + (m2 + m3)).  The hardware
+// reciprocal keeps the 20-iteration chain short (the correctly rounded one is
+// a long instruction sequence); its error is within 1 ulp per step.
+__device__ __forceinline__ float post_and_sinkhorn(float z, const float *bias, const float *mix_scales,
+                                                   const Scalars &s) {
+    const int lane = threadIdx.x & 31;
+    const float a_res = mix_scales[2];
+    float M[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float ze = __shfl_sync(0xffffffffu, z, 8 + e);
+        M[e] = expf(a_res * ze + bias[8 + e]);
     }
-    const int e = (lane - 8) & 15;
-    const int a = e >> 2, c = e & 3;
-    const int rbase = 8 + 4 * a, cbase = 8 + c;
     for (int it = 0; it < s.sinkhorn_iters; ++it) {
-        float m0 = __shfl_sync(0xffffffffu, v, rbase + 0);
-        float m1 = __shfl_sync(0xffffffffu, v, rbase + 1);
-        float m2 = __shfl_sync(0xffffffffu, v, rbase + 2);
-        float m3 = __shfl_sync(0xffffffffu, v, rbase + 3);
-        float rs = (m0 + m1) + (m2 + m3);
-        if (lane >= 8 && lane < 24) v = v / (rs + s.sinkhorn_eps);
-        m0 = __shfl_sync(0xffffffffu, v, cbase + 0);
-        m1 = __shfl_sync(0xffffffffu, v, cbase + 4);
-        m2 = __shfl_sync(0xffffffffu, v, cbase + 8);
-        m3 = __shfl_sync(0xffffffffu, v, cbase + 12);
-        float cs = (m0 + m1) + (m2 + m3);
-        if (lane >= 8 && lane < 24) v = v / (cs + s.sinkhorn_eps);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float inv = rcp_approx(((M[4 * a] + M[4 * a + 1]) + (M[4 * a + 2] + M[4 * a + 3])) + s.sinkhorn_eps);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) M[4 * a + c] *= inv;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float inv = rcp_approx(((M[c] + M[4 + c]) + (M[8 + c] + M[12 + c])) + s.sinkhorn_eps);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) M[4 * a + c] *= inv;
+        }
     }
+    float v = 0.f;
+    if (lane >= 4 && lane < 8) v = s.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        if (lane == 8 + e) v = M[e];
     return v;
+}
+
+// All three heads: lanes 0-3 pre, 4-7 post, 8-23 residual mix.
+__device__ __forceinline__ float heads_and_sinkhorn(float z, const float *bias, const float *mix_scales,
+                                                    const Scalars &s) {
+    const int lane = threadIdx.x & 31;
+    const float p = pre_head(z, bias, mix_scales);
+    const float q = post_and_sinkhorn(z, bias, mix_scales, s);
+    return lane < 4 ? p : q;
 }
 
 // Deterministic warp sum (fixed xor-tree order).

@@ -59,6 +59,14 @@ int fused_slice(int H, int C);                     // hidden elements per CTA (m
 size_t fused_pack_bytes(int H, int C);             // packed phi fragments
 size_t fused_smem_bytes(int H, int C, int G);      // dynamic shared memory per CTA
 cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
+// phi [4H][24] fp32 -> mma A fragments for a cluster of C CTAs of slice Hs
+void launch_pack_phi(const float *phi, int H, int C, int Hs, uint4 *out, int64_t total, cudaStream_t stream);
+
+// Cluster-of-16 schedule with phi resident in tensor memory (kernels_fused_tmem.cu).
+int fused_tmem_slice(int H);
+bool fused_tmem_supported(int H);
+size_t fused_tmem_pack_bytes(int H);
+cudaError_t launch_fused_tmem(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);

@@ -60,14 +60,17 @@ def check_workload(mhc, w, schedule="auto"):
     assert not msgs, "\n".join(msgs)
 
 
+ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16"]
+
+
 @pytest.mark.parametrize("name", ["tiny", "decode_verify", "mid_batch"])
-@pytest.mark.parametrize("schedule", ["auto", "split", "cluster"])
+@pytest.mark.parametrize("schedule", ALL_SCHEDULES)
 def test_workload_parity(mhc, name, schedule):
     check_workload(mhc, synth.WORKLOADS[name], schedule)
 
 
 @pytest.mark.parametrize("T,H", [(1, 8), (3, 24), (5, 264), (17, 1000), (33, 2056), (130, 520)])
-@pytest.mark.parametrize("schedule", ["auto", "split", "cluster"])
+@pytest.mark.parametrize("schedule", ALL_SCHEDULES)
 def test_ragged_shapes(mhc, T, H, schedule):
     check_workload(mhc, synth.Workload(f"ragged_{T}x{H}", T, H, 100 + T, token_scale=True), schedule)
 
@@ -124,7 +127,7 @@ def test_long_prefill_sampled_parity_and_invariants(mhc):
     assert bool(((ms2 - 1).abs() < 2e-2).all()), float((ms2 - 1).abs().max())
 
 
-@pytest.mark.parametrize("schedule", ["split", "cluster"])
+@pytest.mark.parametrize("schedule", ALL_SCHEDULES[1:])
 def test_fused_equals_post_then_pre_bitwise(mhc, schedule):
     mhc.set_schedule(schedule)
     try:
