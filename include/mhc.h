@@ -93,8 +93,11 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_CLUSTER = 2,     /* one pass over HBM, clusters split the hidden dim; default geometry */
     MHC_SCHEDULE_CLUSTER_8x16 = 3,/* clusters of 8 CTAs, 16 tokens per group, 1 CTA per SM */
     MHC_SCHEDULE_CLUSTER_8x8 = 4, /* clusters of 8 CTAs, 8 tokens per group, 2 CTAs per SM */
-    MHC_SCHEDULE_CLUSTER16 = 5    /* clusters of 16 CTAs, 16 tokens per group, phi resident in
+    MHC_SCHEDULE_CLUSTER16 = 5,   /* clusters of 16 CTAs, 16 tokens per group, phi resident in
                                      tensor memory, next group's rows fetched by bulk async copies */
+    MHC_SCHEDULE_PIPE = 6         /* clusters of 16 CTAs, 8 tokens per group, TMA tensor copies into a
+                                     triple buffer, point-to-point DSMEM messages, no cluster barrier
+                                     in the steady state */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -67,6 +67,12 @@ int fused_tmem_slice(int H);
 bool fused_tmem_supported(int H);
 size_t fused_tmem_pack_bytes(int H);
 cudaError_t launch_fused_tmem(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
+
+// Pipelined cluster-of-16 schedule (kernels_pipe.cu).
+int pipe_slice(int H);
+bool pipe_supported(int H);
+size_t pipe_pack_bytes(int H);
+cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
