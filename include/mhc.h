@@ -95,9 +95,11 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_CLUSTER_8x8 = 4, /* clusters of 8 CTAs, 8 tokens per group, 2 CTAs per SM */
     MHC_SCHEDULE_CLUSTER16 = 5,   /* clusters of 16 CTAs, 16 tokens per group, phi resident in
                                      tensor memory, next group's rows fetched by bulk async copies */
-    MHC_SCHEDULE_PIPE = 6         /* clusters of 16 CTAs, 8 tokens per group, TMA tensor copies into a
+    MHC_SCHEDULE_PIPE = 6,        /* clusters of 16 CTAs, 8 tokens per group, TMA tensor copies into a
                                      triple buffer, point-to-point DSMEM messages, no cluster barrier
                                      in the steady state */
+    MHC_SCHEDULE_PIPE2 = 7        /* as PIPE, with the projection on tcgen05.mma (phi resident in
+                                     tensor memory as the A operand) and the Sinkhorn batched at the end */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -152,6 +152,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr)
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -186,34 +197,35 @@ struct Layout {
     __host__ __device__ size_t rec_off() const { return gram_off() + (size_t)kWorkers * 12 * 4; }     // [8][36]
     __host__ __device__ size_t recv_off() const { return rec_off() + (size_t)kG * kRec * 4; }         // [16][36]
     __host__ __device__ size_t prein_off() const { return recv_off() + (size_t)kC * kRec * 4; }       // [2][8][8]
-    __host__ __device__ size_t bar_off() const { return prein_off() + 2 * kG * 8 * 4; }
+    __host__ __device__ size_t gam_off() const { return prein_off() + 2 * kG * 8 * 4; }       // [Hs] bf16
+    __host__ __device__ size_t bar_off() const { return gam_off() + (size_t)nHB * 64 * 2; }
     // full[3], free[3], part_full, pre_full[2]
     __host__ __device__ size_t tmem_off() const { return bar_off() + 9 * 8; }
     __host__ __device__ size_t bytes() const { return tmem_off() + 8; }
 };
 
-__device__ __forceinline__ uint32_t r_swz(int hb, int t, int j, int c16) {
-    const int row = t * 4 + j;
+// R box rows: stream-major (row = j*8 + t, the eight tokens of one stream are
+// consecutive rows, so an ldmatrix over 8 tokens is conflict-free) when the
+// tensor map could be encoded with the streams as the outer dimension,
+// otherwise token-major (row = t*4 + j).
+__device__ __forceinline__ uint32_t r_swz(int hb, int t, int j, int c16, bool jmajor) {
+    const int row = jmajor ? j * 8 + t : t * 4 + j;
     return (uint32_t)(hb * 4096 + row * 128 + ((c16 ^ (row & 7)) << 4));
 }
 __device__ __forceinline__ uint32_t y_swz(int hb, int t, int c16) {
     return (uint32_t)(hb * 1024 + t * 128 + ((c16 ^ (t & 7)) << 4));
 }
 
-// Gram index order: (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-__device__ __forceinline__ void gram_acc(const float (&rf)[kHC][8], float (&gm)[10]) {
+// Gram index order: (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3).
+// Even and odd elements accumulate in the two halves of packed fp32 pairs.
+__device__ __forceinline__ void gram_acc(const float (&rf)[kHC][8], float2 (&gm)[10]) {
+    constexpr int ia[10] = {0, 1, 2, 3, 0, 0, 0, 1, 1, 2}, ib[10] = {0, 1, 2, 3, 1, 2, 3, 2, 3, 3};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        gm[0] = fmaf(rf[0][e], rf[0][e], gm[0]);
-        gm[1] = fmaf(rf[1][e], rf[1][e], gm[1]);
-        gm[2] = fmaf(rf[2][e], rf[2][e], gm[2]);
-        gm[3] = fmaf(rf[3][e], rf[3][e], gm[3]);
-        gm[4] = fmaf(rf[0][e], rf[1][e], gm[4]);
-        gm[5] = fmaf(rf[0][e], rf[2][e], gm[5]);
-        gm[6] = fmaf(rf[0][e], rf[3][e], gm[6]);
-        gm[7] = fmaf(rf[1][e], rf[2][e], gm[7]);
-        gm[8] = fmaf(rf[1][e], rf[3][e], gm[8]);
-        gm[9] = fmaf(rf[2][e], rf[3][e], gm[9]);
+    for (int e = 0; e < 8; e += 2) {
+#pragma unroll
+        for (int q = 0; q < 10; ++q)
+            gm[q] = __ffma2_rn(make_float2(rf[ia[q]][e], rf[ia[q]][e + 1]),
+                               make_float2(rf[ib[q]][e], rf[ib[q]][e + 1]), gm[q]);
     }
 }
 
@@ -225,7 +237,7 @@ template <bool kPost>
 __global__ void __launch_bounds__(kNT, 1)
 pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi_pack,
             const float *__restrict__ bias, const float *__restrict__ mix_scales,
-            const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H, int Hs,
+            const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H, int Hs, bool jmajor,
             uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
             float *__restrict__ post_out, float *__restrict__ res_out, unsigned int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -246,6 +258,7 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off());
     uint64_t *full = bars, *freeb = bars + 3, *part_full = bars + 6, *pre_full = bars + 7;
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.tmem_off());
+    unsigned char *sGam = smem + L.gam_off();
 
     const int h0 = c * Hs;
     const int nvec = Hs / kVec;                          // <= 64
@@ -282,6 +295,11 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
     const uint32_t tw = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * spw * kColsPerStep);
     const int s_begin = min(S, spw * warp), s_end = min(S, spw * (warp + 1));
     if (!control) {
+        // this CTA's slice of the RMSNorm weight (zero beyond H)
+        for (int v = tid; v < nvec; v += kWorkers * 32) {
+            const int h = h0 + v * kVec;
+            *reinterpret_cast<uint4 *>(sGam + v * 16) = h < H ? ld_ro(gamma + h) : make_uint4(0u, 0u, 0u, 0u);
+        }
         const uint4 *pack = phi_pack + (size_t)c * S * 96;
         for (int s = s_begin; s < s_end; ++s) {
             uint32_t r[16];
@@ -312,7 +330,10 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
         const int64_t t0 = (int64_t)(cid + (int64_t)it * nclusters) * kG;
         mbar_arrive_expect_tx(&full[b], expect_bytes);
         for (int hb = 0; hb < nHB; ++hb) {
-            tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, 0, (int)t0, &full[b]);
+            if (jmajor)
+                tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, (int)t0, 0, &full[b]);
+            else
+                tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, 0, (int)t0, &full[b]);
             if (kPost) tma_load_2d(smem + L.y_off(yb) + hb * 1024, &maps.Y, h0 + hb * 64, (int)t0, &full[b]);
         }
         if (kPost) {
@@ -408,9 +429,10 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                 float rf[kHC][8], x[8];
 #pragma unroll
                 for (int j = 0; j < kHC; ++j)
-                    unpack8(*reinterpret_cast<const uint4 *>(rb + r_swz(v >> 3, t, j, v & 7)), rf[j]);
-                combine_vec8(rf, pre, x);
-                st_stream(X_out + (t0 + t) * (int64_t)H + h, norm_vec8(x, rstd, ld_ro(gamma + h)));
+                    unpack8(*reinterpret_cast<const uint4 *>(rb + r_swz(v >> 3, t, j, v & 7, jmajor)), rf[j]);
+                combine_vec8_x2(rf, pre, x);
+                st_stream(X_out + (t0 + t) * (int64_t)H + h,
+                          norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + v * 16)));
             }
             fence_proxy_async_smem();  // the buffer is refilled by TMA after this
             __syncwarp();
@@ -429,20 +451,22 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                 const int t = warp >> 1, half = warp & 1;
                 const int nh = (nvec + 1) >> 1;
                 const int v = half * nh + lane;
-                float gm[10] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float2 gm2[10];
+#pragma unroll
+                for (int q = 0; q < 10; ++q) gm2[q] = make_float2(0.f, 0.f);
                 if (lane < nh && v < nvec) {
                     const int hb = v >> 3, ch = v & 7;
                     float rf[kHC][8];
                     if (kPost) {
                         uint4 r4[kHC], o[kHC];
 #pragma unroll
-                        for (int j = 0; j < kHC; ++j) r4[j] = *reinterpret_cast<const uint4 *>(rb + r_swz(hb, t, j, ch));
+                        for (int j = 0; j < kHC; ++j) r4[j] = *reinterpret_cast<const uint4 *>(rb + r_swz(hb, t, j, ch, jmajor));
                         const uint4 y = *reinterpret_cast<const uint4 *>(smem + L.y_off(yb) + y_swz(hb, t, ch));
                         const float *cb = reinterpret_cast<const float *>(smem + L.comb_off(yb)) + t * 16;
                         const float *pb = reinterpret_cast<const float *>(smem + L.post_off(yb)) + t * 4;
-                        post_vec8(r4, y, cb, pb, o, rf);
+                        post_vec8_x2(r4, y, cb, pb, o, rf);
 #pragma unroll
-                        for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(rb + r_swz(hb, t, j, ch)) = o[j];
+                        for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(rb + r_swz(hb, t, j, ch, jmajor)) = o[j];
                         const int h = h0 + v * kVec;
                         if (t0 + t < T && h < H) {
                             const int64_t base = (t0 + t) * kHC * (int64_t)H + h;
@@ -452,12 +476,13 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                     } else {
 #pragma unroll
                         for (int j = 0; j < kHC; ++j)
-                            unpack8(*reinterpret_cast<const uint4 *>(rb + r_swz(hb, t, j, ch)), rf[j]);
+                            unpack8(*reinterpret_cast<const uint4 *>(rb + r_swz(hb, t, j, ch, jmajor)), rf[j]);
                     }
-                    gram_acc(rf, gm);
+                    gram_acc(rf, gm2);
                 }
+                float gm[10];
 #pragma unroll
-                for (int e = 0; e < 10; ++e) gm[e] = warp_sum(gm[e]);
+                for (int e = 0; e < 10; ++e) gm[e] = warp_sum(gm2[e].x + gm2[e].y);
                 if (lane == 0) {
 #pragma unroll
                     for (int e = 0; e < 10; ++e) sGram[warp * 12 + e] = gm[e];
@@ -474,13 +499,30 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                     for (int q = 0; q < 4; ++q) acc[mt][q] = 0.f;
                 const uint32_t rb32 = smem_u32(rb);
                 const int lt = lane & 7, lk = 8 * ((lane >> 3) & 1);
-                for (int s = s_begin; s < s_end; ++s) {
-                    uint32_t a[16];
-                    tmem_ld16(tw + (uint32_t)((s - s_begin) * kColsPerStep), a);
+                auto bfrag = [&](int s, uint32_t &b0, uint32_t &b1) {
                     const int kk = 16 * s + lk;
                     const int j = kk / Hs, h = kk % Hs;
+                    ldmatrix_x2(rb32 + r_swz(h >> 6, lt, j, (h & 63) >> 3, jmajor), b0, b1);
+                };
+                int s = s_begin;
+                for (; s + 1 < s_end; s += 2) {  // two k16 steps per tensor-memory load
+                    uint32_t a[32];
+                    tmem_ld32(tw + (uint32_t)((s - s_begin) * kColsPerStep), a);
+                    uint32_t b0, b1, b2, b3;
+                    bfrag(s, b0, b1);
+                    bfrag(s + 1, b2, b3);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+                        mma_bf16(acc[mt], a[16 + 4 * mt], a[17 + 4 * mt], a[18 + 4 * mt], a[19 + 4 * mt], b2, b3);
+                }
+                if (s < s_end) {
+                    uint32_t a[16];
+                    tmem_ld16(tw + (uint32_t)((s - s_begin) * kColsPerStep), a);
                     uint32_t b0, b1;
-                    ldmatrix_x2(rb32 + r_swz(h >> 6, lt, j, (h & 63) >> 3), b0, b1);
+                    bfrag(s, b0, b1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
@@ -588,12 +630,20 @@ cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t s
     PipeMaps maps;
     std::memset(&maps, 0, sizeof maps);
     const cuuint64_t H = (cuuint64_t)a.H, T = (cuuint64_t)a.T;
-    {   // R [T][4][H] bf16 as (h, j, t), box 64 x 4 x 8, 128-byte swizzle
-        const cuuint64_t dims[3] = {H, 4, T}, strides[2] = {H * 2, H * 8};
-        const cuuint32_t box[3] = {64, 4, (cuuint32_t)kG};
-        if ((e = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-            return e;
+    bool jmajor = true;
+    {   // R [T][4][H] bf16 as (h, t, j) (box 64 x 8 x 4, stream-major rows in shared memory);
+        // if the encoder refuses the non-monotonic strides, as (h, j, t) (box 64 x 4 x 8)
+        const cuuint64_t dims[3] = {H, T, 4}, strides[2] = {H * 8, H * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kG, 4};
+        if (encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess) {
+            jmajor = false;
+            const cuuint64_t dims2[3] = {H, 4, T}, strides2[2] = {H * 2, H * 8};
+            const cuuint32_t box2[3] = {64, 4, (cuuint32_t)kG};
+            if ((e = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims2, strides2, box2,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+                return e;
+        }
     }
     if (post) {
         const cuuint64_t dy[2] = {H, T}, sy[1] = {H * 2};
@@ -654,7 +704,7 @@ cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t s
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
     return cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                              a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, status);
+                              a.H, Hs, jmajor, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, status);
 }
 
 }  // namespace mhc

@@ -78,6 +78,35 @@ __device__ __forceinline__ void post_vec8(const uint4 (&r)[kHC], uint4 y, const 
     }
 }
 
+// Same arithmetic as post_vec8 on packed fp32 pairs (__fmul2_rn/__ffma2_rn):
+// each half of a packed operation is the same IEEE operation, so the results
+// are bit-identical to post_vec8; half the instructions.
+__device__ __forceinline__ void post_vec8_x2(const uint4 (&r)[kHC], uint4 y, const float *comb,
+                                             const float *post, uint4 (&out)[kHC], float (&rf)[kHC][8]) {
+    float R[kHC][8], Y[8];
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) unpack8(r[j], R[j]);
+    unpack8(y, Y);
+#pragma unroll
+    for (int i = 0; i < kHC; ++i) {
+        float acc[8];
+        const float2 p2 = make_float2(post[i], post[i]);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            float2 a2 = __fmul2_rn(p2, make_float2(Y[e], Y[e + 1]));
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) {
+                const float c = comb[j * kHC + i];
+                a2 = __ffma2_rn(make_float2(c, c), make_float2(R[j][e], R[j][e + 1]), a2);
+            }
+            acc[e] = a2.x;
+            acc[e + 1] = a2.y;
+        }
+        out[i] = pack8_rn(acc);
+        unpack8(out[i], rf[i]);
+    }
+}
+
 // ---- step (4): combine ------------------------------------------------------
 // X[h] = sum_i pre[i] * R'[i][h], fp32: pre0*R0, then fma with i = 1, 2, 3.
 __device__ __forceinline__ void combine_vec8(const float (&rf)[kHC][8], const float (&pre)[kHC],
@@ -89,6 +118,20 @@ __device__ __forceinline__ void combine_vec8(const float (&rf)[kHC][8], const fl
         a = fmaf(pre[2], rf[2][e], a);
         a = fmaf(pre[3], rf[3][e], a);
         x[e] = a;
+    }
+}
+
+// combine_vec8 on packed fp32 pairs; bit-identical to combine_vec8.
+__device__ __forceinline__ void combine_vec8_x2(const float (&rf)[kHC][8], const float (&pre)[kHC],
+                                                float (&x)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float2 a = __fmul2_rn(make_float2(pre[0], pre[0]), make_float2(rf[0][e], rf[0][e + 1]));
+        a = __ffma2_rn(make_float2(pre[1], pre[1]), make_float2(rf[1][e], rf[1][e + 1]), a);
+        a = __ffma2_rn(make_float2(pre[2], pre[2]), make_float2(rf[2][e], rf[2][e + 1]), a);
+        a = __ffma2_rn(make_float2(pre[3], pre[3]), make_float2(rf[3][e], rf[3][e + 1]), a);
+        x[e] = a.x;
+        x[e + 1] = a.y;
     }
 }
 
@@ -116,24 +159,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
-// post and residual-mix heads.  Lanes 4-7 return post[lane-4]; lanes 8-23
-// return the Sinkhorn-normalised residual mix entry e = lane - 8 (row a = e/4,
-// column c = e%4).  Every lane gathers the 16 logits and runs the iteration on
-// the whole 4x4 matrix in registers (no shuffles inside the loop): each row,
-// then each column, is multiplied by the reciprocal of (sum + sinkhorn_eps);
-// sums are taken in the order ((m0 + m1) + (m2 + m3)).  The hardware
-// reciprocal keeps the 20-iteration chain short (the correctly rounded one is
-// a long instruction sequence); its error is within 1 ulp per step.
-__device__ __forceinline__ float post_and_sinkhorn(float z, const float *bias, const float *mix_scales,
-                                                   const Scalars &s) {
-    const int lane = threadIdx.x & 31;
-    const float a_res = mix_scales[2];
-    float M[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const float ze = __shfl_sync(0xffffffffu, z, 8 + e);
-        M[e] = expf(a_res * ze + bias[8 + e]);
-    }
+// Sinkhorn normalisation of one positive 4x4 matrix held in registers
+// (row-major M[4a+c]): sinkhorn_iters times, each row then each column is
+// multiplied by the reciprocal of (sum + sinkhorn_eps); sums are taken in the
+// order ((m0 + m1) + (m2 + m3)).  The hardware reciprocal keeps the dependent
+// chain short (the correctly rounded one is a long instruction sequence); its
+// error is within 1 ulp per step.
+__device__ __forceinline__ void sinkhorn16(float (&M)[16], const Scalars &s) {
     for (int it = 0; it < s.sinkhorn_iters; ++it) {
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
@@ -148,6 +180,23 @@ __device__ __forceinline__ float post_and_sinkhorn(float z, const float *bias, c
             for (int a = 0; a < 4; ++a) M[4 * a + c] *= inv;
         }
     }
+}
+
+// post and residual-mix heads.  Lanes 4-7 return post[lane-4]; lanes 8-23
+// return the Sinkhorn-normalised residual mix entry e = lane - 8 (row a = e/4,
+// column c = e%4).  Every lane gathers the 16 logits and runs sinkhorn16 on
+// the whole 4x4 matrix in registers.
+__device__ __forceinline__ float post_and_sinkhorn(float z, const float *bias, const float *mix_scales,
+                                                   const Scalars &s) {
+    const int lane = threadIdx.x & 31;
+    const float a_res = mix_scales[2];
+    float M[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float ze = __shfl_sync(0xffffffffu, z, 8 + e);
+        M[e] = expf(a_res * ze + bias[8 + e]);
+    }
+    sinkhorn16(M, s);
     float v = 0.f;
     if (lane >= 4 && lane < 8) v = s.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
 #pragma unroll

@@ -73,6 +73,13 @@ int pipe_slice(int H);
 bool pipe_supported(int H);
 size_t pipe_pack_bytes(int H);
 cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
+
+// Pipelined cluster-of-16 schedule with the projection on tcgen05 (kernels_pipe2.cu).
+int pipe2_slice(int H);
+bool pipe2_supported(int H);
+size_t pipe2_pack_bytes(int H);
+size_t pipe2_stash_bytes(int64_t T);
+cudaError_t launch_pipe2(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
