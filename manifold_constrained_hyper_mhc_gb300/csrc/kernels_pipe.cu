@@ -229,6 +229,65 @@ __device__ __forceinline__ void gram_acc(const float (&rf)[kHC][8], float2 (&gm)
     }
 }
 
+// Warp sum of 10 per-lane values, as a butterfly reduce-scatter (12 shuffles
+// instead of 50): each level hands half of the values still held to the
+// partner lane and adds the half it keeps.  Afterwards lane l holds the total
+// of value idx(l) (see gram_lane_index), or padding; fixed order.
+__device__ __forceinline__ float gram_reduce_scatter(const float (&v)[10]) {
+    const int lane = threadIdx.x & 31;
+    // level 1 (xor 16): 10 -> 5
+    float a[6];
+    {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const float keep = hi ? v[5 + i] : v[i], give = hi ? v[i] : v[5 + i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+        }
+        a[5] = 0.f;
+    }
+    // level 2 (xor 8): 6 -> 3
+    float b[4];
+    {
+        const bool hi = lane & 8;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const float keep = hi ? a[3 + i] : a[i], give = hi ? a[i] : a[3 + i];
+            b[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+        }
+        b[3] = 0.f;
+    }
+    // level 3 (xor 4): 4 -> 2
+    float c2[2];
+    {
+        const bool hi = lane & 4;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float keep = hi ? b[2 + i] : b[i], give = hi ? b[i] : b[2 + i];
+            c2[i] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+        }
+    }
+    // level 4 (xor 2): 2 -> 1
+    float d;
+    {
+        const bool hi = lane & 2;
+        const float keep = hi ? c2[1] : c2[0], give = hi ? c2[0] : c2[1];
+        d = keep + __shfl_xor_sync(0xffffffffu, give, 2);
+    }
+    // level 5 (xor 1): both lanes end with the full sum
+    return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+// Which of the 10 values lane l holds after gram_reduce_scatter (-1: padding).
+__device__ __forceinline__ int gram_lane_index(int lane) {
+    // level 2 leaves values {0,1,2} (bit 3 clear) or {3,4} (bit 3 set) of each half,
+    // levels 3-4 pick one of them (or padding) by bits 2 and 1
+    const int base = (lane & 16) ? 5 : 0;
+    const bool upper = lane & 8;
+    const int bi = ((lane & 4) ? 2 : 0) + ((lane & 2) ? 1 : 0);
+    if (bi >= (upper ? 2 : 3)) return -1;
+    return base + (upper ? 3 : 0) + bi;
+}
+
 struct PipeMaps {
     CUtensorMap R, Y, comb, post;
 };
@@ -239,7 +298,8 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
             const float *__restrict__ bias, const float *__restrict__ mix_scales,
             const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H, int Hs, bool jmajor,
             uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
-            float *__restrict__ post_out, float *__restrict__ res_out, unsigned int *__restrict__ status) {
+            float *__restrict__ post_out, float *__restrict__ res_out, float *__restrict__ zstash,
+            unsigned int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzled TMA boxes need a 1024-byte aligned base (1 KB of slack is allocated)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -402,12 +462,12 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                                                    __float_as_uint(pre[2]), __float_as_uint(pre[3])));
                 st_async16(raddr + 16, rbar, make_uint4(__float_as_uint(rstd), 0u, 0u, 0u));
             }
-            const float v = post_and_sinkhorn(z, bias, mix_scales, sc);
             if (valid) {
                 const int64_t t = t0 + g;
                 if (lane < 4) pre_out[t * 4 + lane] = p;
-                else if (lane < 8) post_out[t * 4 + lane - 4] = v;
-                else if (lane < 24) res_out[t * 16 + lane - 8] = v;
+                else if (lane < 8)
+                    post_out[t * 4 + lane - 4] = sc.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
+                else if (lane < 24) zstash[t * 16 + lane - 8] = z;  // residual-mix logits, normalised at the end
             }
         }
     } else {
@@ -482,21 +542,20 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                 }
                 float gm[10];
 #pragma unroll
-                for (int e = 0; e < 10; ++e) gm[e] = warp_sum(gm2[e].x + gm2[e].y);
-                if (lane == 0) {
-#pragma unroll
-                    for (int e = 0; e < 10; ++e) sGram[warp * 12 + e] = gm[e];
-                }
+                for (int e = 0; e < 10; ++e) gm[e] = gm2[e].x + gm2[e].y;
+                const float tot = gram_reduce_scatter(gm);
+                const int gi = gram_lane_index(lane);
+                if (gi >= 0 && (lane & 1) == 0) sGram[warp * 12 + gi] = tot;
             }
             workers_sync();
 
             // ---- P2: projection partials of this warp's k16 steps for the 8 tokens
             {
-                float acc[3][4];
+                float acc[3][4], acc2[3][4];  // even and odd k16 steps accumulate separately
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[mt][q] = 0.f;
+                    for (int q = 0; q < 4; ++q) acc[mt][q] = acc2[mt][q] = 0.f;
                 const uint32_t rb32 = smem_u32(rb);
                 const int lt = lane & 7, lk = 8 * ((lane >> 3) & 1);
                 auto bfrag = [&](int s, uint32_t &b0, uint32_t &b1) {
@@ -516,7 +575,7 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                     for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[16 + 4 * mt], a[17 + 4 * mt], a[18 + 4 * mt], a[19 + 4 * mt], b2, b3);
+                        mma_bf16(acc2[mt], a[16 + 4 * mt], a[17 + 4 * mt], a[18 + 4 * mt], a[19 + 4 * mt], b2, b3);
                 }
                 if (s < s_end) {
                     uint32_t a[16];
@@ -527,6 +586,10 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
                 }
+#pragma unroll
+                for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[mt][q] += acc2[mt][q];
                 float *zw = sZ + (size_t)warp * kG * kNumMix;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -536,6 +599,8 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                     zw[t * kNumMix + gid + 16] = acc[1][e] + acc[2][2 + e];
                 }
             }
+            // ---- combine + RMSNorm of the previous group (overlaps other warps' MMA chains)
+            if (it >= 1) combine(it - 1);
             workers_sync();
 
             // ---- records: 24 logits (sum over the 16 warps, fixed order) + 10 Gram entries
@@ -559,13 +624,36 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
                 st_async16(raddr, rbar, val);
             }
 
-            // ---- combine + RMSNorm of the previous group
-            if (it >= 1) combine(it - 1);
         }
         if (n_it >= 1) combine(n_it - 1);
     }
 
     cluster.sync();  // all messages delivered; no CTA leaves while others may still write to it
+
+    // ---- Sinkhorn of the tokens this CTA owned, one token per thread
+    {
+        const int first = c >= 8 ? 1 : 0;
+        const int nown = n_it > first ? (n_it - first + 1) / 2 : 0;
+        for (int k = tid; k < nown; k += kNT) {
+            const int it = first + 2 * k;
+            const int64_t t = (int64_t)(cid + (int64_t)it * nclusters) * kG + (c - 8 * (it & 1));
+            if (t >= T) continue;
+            float M[16];
+            const float4 *zs = reinterpret_cast<const float4 *>(zstash + t * 16);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float4 f = zs[x];
+                M[4 * x] = f.x; M[4 * x + 1] = f.y; M[4 * x + 2] = f.z; M[4 * x + 3] = f.w;
+            }
+            const float a_res = mix_scales[2];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) M[e] = expf(a_res * M[e] + bias[8 + e]);
+            sinkhorn16(M, sc);
+            float4 *ro = reinterpret_cast<float4 *>(res_out + t * 16);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) ro[x] = make_float4(M[4 * x], M[4 * x + 1], M[4 * x + 2], M[4 * x + 3]);
+        }
+    }
     const bool any_dead = __any_sync(0xffffffffu, dead);
     if (any_dead && lane == 0) atomicOr(status, 1u);
     tmem_fence_before();
@@ -620,7 +708,9 @@ size_t pipe_pack_bytes(int H) {
     return (size_t)kC * (kHC * Hs / 16) * 96 * 16;
 }
 
-cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t stream) {
+size_t pipe_stash_bytes(int64_t T) { return (size_t)T * 16 * 4; }
+
+cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream) {
     if (!pipe_supported(a.H)) return cudaErrorInvalidValue;
     const int Hs = pipe_slice(a.H);
     const bool post = a.R_out != nullptr;
@@ -704,7 +794,7 @@ cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t s
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
     return cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                              a.H, Hs, jmajor, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, status);
+                              a.H, Hs, jmajor, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status);
 }
 
 }  // namespace mhc

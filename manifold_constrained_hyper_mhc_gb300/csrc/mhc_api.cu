@@ -124,7 +124,7 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
         for (const ClusterGeom *g : {&kGeom8x16, &kGeom8x8})
             sched = std::max(sched, mhc::fused_pack_bytes((int)H, g->C));
         sched = std::max(sched, mhc::fused_tmem_pack_bytes((int)H));
-        sched = std::max(sched, mhc::pipe_pack_bytes((int)H));
+        sched = std::max(sched, ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe_stash_bytes(T));
         sched = std::max(sched, ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe2_stash_bytes(T));
     }
     size_t b = mhc::kControlBytes + sched;
@@ -247,9 +247,11 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.R_out = fused ? residual_out : nullptr;
             a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
             a.res_out = comb_res_mix_out;
-            a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            char *ws = static_cast<char *>(workspace) + mhc::kControlBytes;
+            a.phi_pack = reinterpret_cast<uint4 *>(ws);
+            float *zstash = reinterpret_cast<float *>(ws + ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)));
             a.C = 16; a.G = 8;
-            e = mhc::launch_pipe(a, static_cast<unsigned int *>(workspace), cs);
+            e = mhc::launch_pipe(a, static_cast<unsigned int *>(workspace), zstash, cs);
             g_launches = 2;
             break;
         }

@@ -72,7 +72,8 @@ cudaError_t launch_fused_tmem(const FusedArgs &a, unsigned int *status, cudaStre
 int pipe_slice(int H);
 bool pipe_supported(int H);
 size_t pipe_pack_bytes(int H);
-cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
+size_t pipe_stash_bytes(int64_t T);
+cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
 
 // Pipelined cluster-of-16 schedule with the projection on tcgen05 (kernels_pipe2.cu).
 int pipe2_slice(int H);
