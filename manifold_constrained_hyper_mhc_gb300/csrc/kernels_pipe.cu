@@ -551,45 +551,49 @@ pipe_kernel(const __grid_constant__ PipeMaps maps, const uint4 *__restrict__ phi
 
             // ---- P2: projection partials of this warp's k16 steps for the 8 tokens
             {
-                float acc[3][4], acc2[3][4];  // even and odd k16 steps accumulate separately
+                float acc[3][4];
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[mt][q] = acc2[mt][q] = 0.f;
+                    for (int q = 0; q < 4; ++q) acc[mt][q] = 0.f;
                 const uint32_t rb32 = smem_u32(rb);
                 const int lt = lane & 7, lk = 8 * ((lane >> 3) & 1);
-                auto bfrag = [&](int s, uint32_t &b0, uint32_t &b1) {
-                    const int kk = 16 * s + lk;
-                    const int j = kk / Hs, h = kk % Hs;
-                    ldmatrix_x2(rb32 + r_swz(h >> 6, lt, j, (h & 63) >> 3, jmajor), b0, b1);
+                // k = 16 s + lk = j*Hs + h, advanced incrementally (Hs is a multiple of 64, steps of 16
+                // never cross a stream)
+                int sj = (16 * s_begin) / Hs, sh = (16 * s_begin) % Hs;
+                auto bfrag = [&](int j, int h, uint32_t &b0, uint32_t &b1) {
+                    const int hh = h + lk;
+                    ldmatrix_x2(rb32 + r_swz(hh >> 6, lt, j, (hh & 63) >> 3, jmajor), b0, b1);
+                };
+                auto advance = [&]() {
+                    sh += 16;
+                    if (sh >= Hs) { sh -= Hs; ++sj; }
                 };
                 int s = s_begin;
                 for (; s + 1 < s_end; s += 2) {  // two k16 steps per tensor-memory load
                     uint32_t a[32];
                     tmem_ld32(tw + (uint32_t)((s - s_begin) * kColsPerStep), a);
                     uint32_t b0, b1, b2, b3;
-                    bfrag(s, b0, b1);
-                    bfrag(s + 1, b2, b3);
+                    bfrag(sj, sh, b0, b1);
+                    advance();
+                    bfrag(sj, sh, b2, b3);
+                    advance();
                     tmem_wait_ld();
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc2[mt], a[16 + 4 * mt], a[17 + 4 * mt], a[18 + 4 * mt], a[19 + 4 * mt], b2, b3);
+                        mma_bf16(acc[mt], a[16 + 4 * mt], a[17 + 4 * mt], a[18 + 4 * mt], a[19 + 4 * mt], b2, b3);
                 }
                 if (s < s_end) {
                     uint32_t a[16];
                     tmem_ld16(tw + (uint32_t)((s - s_begin) * kColsPerStep), a);
                     uint32_t b0, b1;
-                    bfrag(s, b0, b1);
+                    bfrag(sj, sh, b0, b1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int mt = 0; mt < 3; ++mt) mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b0, b1);
                 }
-#pragma unroll
-                for (int mt = 0; mt < 3; ++mt)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[mt][q] += acc2[mt][q];
                 float *zw = sZ + (size_t)warp * kG * kNumMix;
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
