@@ -98,8 +98,11 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_PIPE = 6,        /* clusters of 16 CTAs, 8 tokens per group, TMA tensor copies into a
                                      triple buffer, point-to-point DSMEM messages, no cluster barrier
                                      in the steady state */
-    MHC_SCHEDULE_PIPE2 = 7        /* as PIPE, with the projection on tcgen05.mma (phi resident in
+    MHC_SCHEDULE_PIPE2 = 7,       /* as PIPE, with the projection on tcgen05.mma (phi resident in
                                      tensor memory as the A operand) and the Sinkhorn batched at the end */
+    MHC_SCHEDULE_WS = 8           /* as PIPE with warp-specialised roles (TMA producer, post,
+                                     projection + Gram on the tensor cores, owner, combine) handing
+                                     groups over through mbarriers, and a 5-deep tile ring */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -126,12 +126,14 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
         sched = std::max(sched, mhc::fused_tmem_pack_bytes((int)H));
         sched = std::max(sched, ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe_stash_bytes(T));
         sched = std::max(sched, ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe2_stash_bytes(T));
+        sched = std::max(sched, ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::ws_stash_bytes(T));
     }
     size_t b = mhc::kControlBytes + sched;
     return (b + 255) & ~size_t(255);
 }
 
 int auto_schedule(int64_t /*T*/, int64_t H) {
+    if (mhc::ws_supported((int)H)) return MHC_SCHEDULE_WS;
     if (mhc::pipe_supported((int)H)) return MHC_SCHEDULE_PIPE;
     return cluster_fits(kGeomDefault, H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
 }
@@ -273,6 +275,24 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             g_launches = 2;
             break;
         }
+        case MHC_SCHEDULE_WS: {
+            if (!mhc::ws_supported((int)H))
+                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the ws schedule", (long long)H);
+            mhc::FusedArgs a{};
+            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
+            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+            a.T = T; a.H = (int)H; a.s = s;
+            a.R_out = fused ? residual_out : nullptr;
+            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.res_out = comb_res_mix_out;
+            char *ws = static_cast<char *>(workspace) + mhc::kControlBytes;
+            a.phi_pack = reinterpret_cast<uint4 *>(ws);
+            float *zstash = reinterpret_cast<float *>(ws + ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)));
+            a.C = 16; a.G = 8;
+            e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
+            g_launches = 2;
+            break;
+        }
         case MHC_SCHEDULE_CLUSTER16: {
             if (!mhc::fused_tmem_supported((int)H))
                 return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster16 schedule", (long long)H);
@@ -367,7 +387,7 @@ mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const f
 
 mhc_status mhc_set_schedule(int schedule) {
     if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER16 &&
-        schedule != MHC_SCHEDULE_PIPE && schedule != MHC_SCHEDULE_PIPE2 &&
+        schedule != MHC_SCHEDULE_PIPE && schedule != MHC_SCHEDULE_PIPE2 && schedule != MHC_SCHEDULE_WS &&
         geom_of(schedule) == nullptr)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);

@@ -81,6 +81,13 @@ bool pipe2_supported(int H);
 size_t pipe2_pack_bytes(int H);
 size_t pipe2_stash_bytes(int64_t T);
 cudaError_t launch_pipe2(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
+// Warp-specialised pipelined cluster-of-16 schedule (kernels_ws.cu).
+int ws_slice(int H);
+bool ws_supported(int H);
+size_t ws_pack_bytes(int H);
+size_t ws_stash_bytes(int64_t T);
+cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);

@@ -60,7 +60,7 @@ def check_workload(mhc, w, schedule="auto"):
     assert not msgs, "\n".join(msgs)
 
 
-ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2"]
+ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws"]
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_verify", "mid_batch"])
