@@ -4,31 +4,33 @@
 // A cluster of 16 CTAs (one per SM) owns groups of G = 8 tokens; CTA c owns
 // the hidden slice [c*Hs, (c+1)*Hs) of each token (Hs a multiple of 64, at
 // most 512).  Each role is its own set of warps, and the roles hand groups to
-// one another through mbarriers only, so no role waits for another role's
-// slowest warp and their latencies overlap:
+// one another through mbarriers, so no role waits for another role's slowest
+// warp and their latencies overlap:
 //
-//   producer (1 warp) : TMA tensor copies of group q (R as 64 x 8 x 4 boxes of
-//                       4 KB, Y as 64 x 8 boxes, the previous mixes) into a
-//                       5-deep ring once the combine has released the slot.
-//   post (8 warps)    : warp t: token t of the group; R' = comb^T R + post Y in
-//                       shared memory (R' overwrites R), R' to HBM.
-//   projection (4)    : warp p: hidden blocks [p*Hs/4, (p+1)*Hs/4) of the
-//                       slice, all four streams.  Per 16 hidden values two
-//                       ldmatrix.x4 load the 8 tokens' R' of streams (0,1) and
-//                       (2,3); the same fragments are the B operand of the
-//                       projection (A = phi^T hi/lo fragments resident in
-//                       tensor memory, mma.sync bf16, fp32 accumulate) and both
-//                       operands of five Gram-matrix MMAs (R'_x . R'_j over the
-//                       hidden values for the stream pairs, of which each token
-//                       keeps its own diagonal entries).  The four warps' partials are summed
-//                       into one 144-byte record per token (24 logits + 10 Gram
-//                       entries) and sent to the token's owner CTA (st.async).
+//   post (7 warps)    : the group's (token, 8-value vector) items, two per
+//                       thread; R' = comb^T R + post Y in shared memory (R'
+//                       overwrites R), R' to HBM.
+//   projection (8)    : warp p: tensor-memory lane quadrant p % 4, half of
+//                       that quadrant's quarter of the slice, all four streams.
+//                       Per 16 hidden values two ldmatrix.x4 load the 8 tokens'
+//                       R' of streams (0,1) and (2,3); the same fragments are the
+//                       B operand of the projection (A = phi^T hi/lo fragments
+//                       resident in tensor memory, mma.sync bf16, fp32
+//                       accumulate) and both operands of six Gram-matrix MMAs
+//                       (R'_i . R'_j over the hidden values for the stream
+//                       pairs, of which each token keeps its own diagonal
+//                       entries).  The eight warps' partials are summed into one
+//                       144-byte record per token (24 logits + 10 Gram entries)
+//                       and sent to the token's owner CTA (st.async).
 //   owner (1 warp)    : for the token this CTA owns in the group: sum the 16
 //                       records, r, the pre and post heads, rstd of the combined
 //                       row from the Gram matrix (sum_h X^2 = pre^T G pre),
 //                       (pre, rstd) to all 16 CTAs; residual-mix logits kept.
 //   combine (4 warps) : X = sum_i pre_i R'_i, RMSNorm * gamma, bf16 to HBM;
-//                       then releases the ring slot to the producer.
+//                       then, the slot's last use being over, one thread issues
+//                       the TMA tensor copies of group q + 5 into it (R as
+//                       64 x 8 x 4 boxes of 4 KB, Y as 64 x 8 boxes, the
+//                       previous mixes).
 // At the end all warps run the Sinkhorn normalisations of the owned tokens,
 // one token per thread.
 //
@@ -40,15 +42,16 @@
 // group can only reach them after the combine of the group 5 earlier.
 //
 // Every mbarrier wait is bounded: on a timeout the CTA sets bit 0 of the
-// status word and stops waiting (later waits give up at once), waits (again
-// bounded) for its own tensor copies in flight, meets the cluster barrier at
-// the end, frees its tensor memory and exits.
+// status word and stops waiting (later waits give up at once), issues no more
+// copies, waits (again bounded) for its copies in flight, meets the cluster
+// barrier at the end, frees its tensor memory and exits.
 #include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "mhc_device.cuh"
 #include "mhc_kernels.h"
@@ -64,24 +67,26 @@ using namespace ptx;
 
 constexpr int kC = 16;                    // CTAs per cluster
 constexpr int kG = 8;                     // tokens per group
-constexpr int kP1 = kG;                   // post warps
-constexpr int kP2 = 4;                    // projection warps (one tensor-memory lane quadrant each)
-constexpr int kCB = 4;                    // combine warps
-constexpr int kWP2 = kP1;                 // first projection warp
-constexpr int kWCB = kP1 + kP2;           // first combine warp
-constexpr int kWOwner = kP1 + kP2 + kCB;  // owner warp
-constexpr int kWProd = kWOwner + 1;       // producer warp
+constexpr int kP1 = 7;                    // post warps 0-6
+constexpr int kWP2 = kP1;                 // projection warps 7-13
+constexpr int kP2 = 7;
+constexpr int kWOwner = kWP2 + kP2;       // owner warp (14)
+constexpr int kWCB = kWOwner + 1;         // combine warps 15-18
+constexpr int kCB = 4;
+constexpr int kWProd = kWCB + kCB;        // producer warp (19)
 constexpr int kNT = (kWProd + 1) * 32;
+constexpr int kMaxB16 = 4 * kP2;          // 16-wide hidden blocks per slice: at most four per projection warp
+constexpr int kP1Items = (kG * kMaxB16 * 2 + kP1 * 32 - 1) / (kP1 * 32);  // post items per thread
+constexpr int kCItems = (kG * kMaxB16 * 2 + kCB * 32 - 1) / (kCB * 32);   // combine items per thread
 constexpr int kNBuf = 5;                  // ring of R / Y / mix tiles
 constexpr int kNPre = 5;                  // (pre, rstd) slots; must be >= kNBuf
 constexpr int kRec = 36;                  // floats per record: 24 logits, 10 Gram entries, 2 pad
 constexpr int kTmemCols = 512;
-constexpr uint32_t kWaitLimit = 1u << 25;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 static_assert(kNPre >= kNBuf, "a (pre, rstd) slot is reused only after the combine of its last group");
-static_assert(kWP2 % 4 == 0, "projection warp p must own tensor-memory lane quadrant p");
 
 __device__ __forceinline__ void bwait(uint64_t *bar, uint32_t parity, bool &dead) {
-    mbar_wait(bar, parity, dead, kWaitLimit);
+    mbar_wait_timed(bar, parity, dead, kWaitLimitNs);
 }
 
 // One k16 step's phi^T fragments (3 m-tiles x 4 registers) from tensor memory columns
@@ -111,6 +116,23 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// D = A x B (no accumulator input)
+__device__ __forceinline__ void mma_bf16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+template <bool kFirst>
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    if constexpr (kFirst)
+        mma_bf16_z(d, a0, a1, a2, a3, b0, b1);
+    else
+        mma_bf16(d, a0, a1, a2, a3, b0, b1);
+}
 
 // ---- shared memory layout ---------------------------------------------------------
 // Ring slot b: R' tile of nHB boxes of [stream 4][token 8][64 hidden] bf16 (4 KB each,
@@ -135,14 +157,21 @@ struct Layout {
     __host__ __device__ size_t bytes() const { return tmem_off() + 8; }
 };
 
-// Byte offset of 16-byte chunk c16 (8 hidden values) of (token t, stream j) in box hb.
-// Box rows are stream-major (row = j*8 + t: the 8 tokens of one stream are consecutive
-// rows, so an 8-token ldmatrix is conflict-free) when the tensor map could be encoded
-// with the streams as the outer dimension, otherwise token-major (row = t*4 + j).
-__device__ __forceinline__ uint32_t r_swz(int hb, int t, int j, int c16, bool jmajor) {
-    const int row = jmajor ? j * 8 + t : t * 4 + j;
-    return (uint32_t)(hb * 4096 + row * 128 + ((c16 ^ (row & 7)) << 4));
+// R tile layout in shared memory.  Rows of 128 bytes (64 hidden values) hold one
+// (stream j, 64-wide hidden block hb, token t); the TMA 128-byte swizzle puts 16-byte
+// chunk c16 of a row at chunk c16 ^ (row % 8), and row % 8 = t in both layouts below,
+// so the 8 tokens of one (j, hb) are 8 consecutive rows and an 8-token ldmatrix is
+// conflict-free.
+//   one box : a single 4-D copy [j 4][hb nHB][t 8][64]  (s_hb = 1024, s_j = nHB*1024)
+//   per hb  : nHB 3-D copies   [hb nHB][j 4][t 8][64]  (s_hb = 4096, s_j = 1024)
+struct RLayout {
+    int s_hb, s_j;
+    bool one_box;
+};
+__device__ __forceinline__ uint32_t r_swz(int hb, int t, int j, int c16, const RLayout &lay) {
+    return (uint32_t)(hb * lay.s_hb + j * lay.s_j + t * 128 + ((c16 ^ t) << 4));
 }
+// Y tile: rows (hb, t), in both layouts.
 __device__ __forceinline__ uint32_t y_swz(int hb, int t, int c16) {
     return (uint32_t)(hb * 1024 + t * 128 + ((c16 ^ (t & 7)) << 4));
 }
@@ -155,7 +184,7 @@ template <bool kPost>
 __global__ void __launch_bounds__(kNT, 1)
 ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pack, const float *__restrict__ bias,
           const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H,
-          int Hs, bool jmajor, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out,
+          int Hs, RLayout lay, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out,
           float *__restrict__ pre_out, float *__restrict__ post_out, float *__restrict__ res_out,
           float *__restrict__ zstash, unsigned int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -175,11 +204,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     uint64_t *full = bars, *postd = bars + kNBuf, *freeb = bars + 2 * kNBuf, *part_full = bars + 3 * kNBuf,
              *pre_full = bars + 3 * kNBuf + 2;
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.tmem_off());
-    // the projection and the combine wait for R' (post mode) or for the tile itself (pre only)
-    uint64_t *rdy = kPost ? postd : full;
 
     const int h0 = c * Hs;
-    const int nvec = Hs / kVec;  // <= 64
+    const int nvec = Hs / kVec;  // <= 56
+    const int nB16 = Hs / 16;    // 16-wide hidden blocks of the slice, <= 28
     const int64_t ngroups = (T + kG - 1) / kG;
     const int nclusters = gridDim.x / kC;
     const int cid = blockIdx.x / kC;
@@ -188,10 +216,13 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     const int first_owned = c >= kG ? 1 : 0;
     const int nown = n_it > first_owned ? (n_it - first_owned + 1) / 2 : 0;
     auto group_t0 = [&](int q) { return (int64_t)(cid + (int64_t)q * nclusters) * kG; };
+    // the 16-wide blocks of projection warp p: [blk0(p), blk0(p) + nblk(p)), at most 4
+    auto nblk = [&](int p) { return nB16 / kP2 + (p < nB16 % kP2 ? 1 : 0); };
+    auto blk0 = [&](int p) { return p * (nB16 / kP2) + min(p, nB16 % kP2); };
     bool dead = false;
 
     // ---- set-up
-    if (warp == kWProd) {
+    if (warp == kWOwner) {
         if (lane == 0) {
             for (int i = 0; i < kNBuf; ++i) {
                 mbar_init(&full[i], 1);
@@ -210,16 +241,22 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     __syncthreads();
     tmem_fence_after();
     const uint32_t tbase = *sTmem;
-    if (warp >= kWP2 && warp < kWCB) {
-        // phi^T fragments of this warp's hidden blocks: column (lb*4 + j)*16 holds the
-        // 3 x 4 registers of k16 step s = j*(Hs/16) + p*nHB + lb
+    // projection warp p = warp - kWP2 keeps the phi^T fragments of its blocks in tensor-memory
+    // lane quadrant warp % 4, after those of the lower projection warps of the same quadrant:
+    // block i, stream j at column col0 + (i*4 + j)*16 (3 x 4 registers of k16 step
+    // s = j*(Hs/16) + blk0(p) + i)
+    uint32_t tq = 0;
+    if (warp >= kWP2 && warp < kWP2 + kP2) {
         const int p = warp - kWP2;
-        const uint32_t tq = tbase + ((uint32_t)(32 * p) << 16);
+        int col0 = 0;
+        for (int p2 = 0; p2 < p; ++p2)
+            if (((p2 + kWP2) & 3) == (warp & 3)) col0 += 64 * nblk(p2);
+        tq = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col0;
         const uint4 *pack = phi_pack + (size_t)c * (kHC * Hs / 16) * 96;
-        for (int lb = 0; lb < nHB; ++lb) {
+        for (int i = 0; i < nblk(p); ++i) {
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
-                const int s = j * (Hs / 16) + p * nHB + lb;
+                const int s = j * nB16 + blk0(p) + i;
                 uint32_t r[16];
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt) {
@@ -227,180 +264,201 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                     r[4 * mt] = a.x; r[4 * mt + 1] = a.y; r[4 * mt + 2] = a.z; r[4 * mt + 3] = a.w;
                 }
                 r[12] = r[13] = r[14] = r[15] = 0u;
-                tmem_st16(tq + (uint32_t)((lb * 4 + j) * 16), r);
+                tmem_st16(tq + (uint32_t)((i * 4 + j) * 16), r);
             }
         }
         tmem_wait_st();
     }
-    if (warp >= kWCB && warp < kWOwner) {
+    if (warp >= kWCB && warp < kWCB + kCB) {
         // this CTA's slice of the RMSNorm weight (zero beyond H)
         for (int v = tid - kWCB * 32; v < nvec; v += kCB * 32) {
             const int h = h0 + v * kVec;
             *reinterpret_cast<uint4 *>(sGam + v * 16) = h < H ? ld_ro(gamma + h) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    if (warp == kWProd && lane == 0) {
+    if (warp == kWOwner && lane == 0) {
         // arm the message barriers for their first phases
         for (int i = 0; i < 2 && i < nown; ++i) mbar_arrive_expect_tx(&part_full[i], kC * kRec * 4);
         for (int i = 0; i < kNPre && i < n_it; ++i) mbar_arrive_expect_tx(&pre_full[i], kG * 32);
     }
     cluster.sync();  // every CTA's barriers exist before any message is sent
 
-    if (warp == kWProd) {
-        // ================================ producer
-        if (lane == 0) {
-            const uint32_t expect_bytes = (uint32_t)nHB * (4096 + (kPost ? 1024 : 0)) + (kPost ? 512 + 128 : 0);
-            int issued = 0;
-            for (int q = 0; q < n_it && !dead; ++q) {
-                const int b = q % kNBuf;
-                if (q >= kNBuf) bwait(&freeb[b], (uint32_t)((q / kNBuf - 1) & 1), dead);
-                if (dead) break;
-                const int t0 = (int)group_t0(q);
-                mbar_arrive_expect_tx(&full[b], expect_bytes);
-                for (int hb = 0; hb < nHB; ++hb) {
-                    if (jmajor)
-                        tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
-                    else
-                        tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, 0, t0, &full[b]);
-                    if (kPost) tma_load_2d(smem + L.y_off(b) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &full[b]);
-                }
-                if (kPost) {
-                    tma_load_2d(smem + L.comb_off(b), &maps.comb, 0, t0, &full[b]);
-                    tma_load_2d(smem + L.post_off(b), &maps.post, 0, t0, &full[b]);
-                }
-                ++issued;
-            }
-            // the copies of the last kNBuf groups have landed (already true unless a wait timed out)
-            bool drained = false;
-            for (int q = issued > kNBuf ? issued - kNBuf : 0; q < issued; ++q)
-                mbar_wait(&full[q % kNBuf], (uint32_t)((q / kNBuf) & 1), drained, kWaitLimit);
-            dead = dead || drained;
-        }
-        __syncwarp();
-    } else if (warp < kP1) {
-        // ================================ post: token t = warp
+    if (warp < kP1) {
+        // ================================ post: items (token, vector) pt + k * 224 of the group
         if (kPost) {
-            const int t = warp;
+            constexpr int kStride = kP1 * 32;
+            // consecutive items are consecutive vectors of one token, so every 8-lane wavefront reads
+            // and writes the 8 chunks of one 128-byte row: conflict-free.  The items are the same in
+            // every group: their offsets are computed once.
+            uint32_t p_roff[kP1Items], p_yoff[kP1Items];
+            int p_t[kP1Items], p_goff[kP1Items];
+#pragma unroll
+            for (int k = 0; k < kP1Items; ++k) {
+                const int item = tid + k * kStride;
+                const int t = item / nvec, v = item % nvec;
+                const bool on = item < kG * nvec && h0 + v * kVec < H;
+                p_t[k] = on ? t : kG;  // kG: no item
+                p_roff[k] = r_swz(v >> 3, t, 0, v & 7, lay);
+                p_yoff[k] = y_swz(v >> 3, t, v & 7);
+                p_goff[k] = t * kHC * H + h0 + v * kVec;
+            }
             for (int q = 0; q < n_it; ++q) {
                 const int b = q % kNBuf;
                 bwait(&full[b], (uint32_t)((q / kNBuf) & 1), dead);
-                const int64_t t0 = group_t0(q);
                 unsigned char *rb = smem + L.r_off(b);
-                float cm[kHC * kHC], pm[kHC];
-                {
-                    const float4 *cb = reinterpret_cast<const float4 *>(smem + L.comb_off(b)) + t * 4;
+                const int64_t t0 = group_t0(q);
+                uint16_t *rrow = R_out + t0 * kHC * (int64_t)H;
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float4 f = cb[x];
-                        cm[4 * x] = f.x; cm[4 * x + 1] = f.y; cm[4 * x + 2] = f.z; cm[4 * x + 3] = f.w;
-                    }
-                    const float4 f = *(reinterpret_cast<const float4 *>(smem + L.post_off(b)) + t);
-                    pm[0] = f.x; pm[1] = f.y; pm[2] = f.z; pm[3] = f.w;
-                }
-                const bool valid_t = t0 + t < T;
-                for (int v = lane; v < nvec; v += 32) {
-                    const int hb = v >> 3, ch = v & 7;
-                    uint4 r4[kHC], o[kHC];
-                    float rf[kHC][8];
+                for (int k = 0; k < kP1Items; ++k) {
+                    const int t = p_t[k];
+                    if (t < kG) {
+                        const float *cb = reinterpret_cast<const float *>(smem + L.comb_off(b)) + t * 16;
+                        const float *pb = reinterpret_cast<const float *>(smem + L.post_off(b)) + t * 4;
+                        unsigned char *rp = rb + p_roff[k];
+                        uint4 r4[kHC], o[kHC];
+                        float rf[kHC][8];
 #pragma unroll
-                    for (int j = 0; j < kHC; ++j) r4[j] = *reinterpret_cast<const uint4 *>(rb + r_swz(hb, t, j, ch, jmajor));
-                    const uint4 y = *reinterpret_cast<const uint4 *>(smem + L.y_off(b) + y_swz(hb, t, ch));
-                    post_vec8_x2(r4, y, cm, pm, o, rf);
+                        for (int j = 0; j < kHC; ++j) r4[j] = *reinterpret_cast<const uint4 *>(rp + j * lay.s_j);
+                        const uint4 y = *reinterpret_cast<const uint4 *>(smem + L.y_off(b) + p_yoff[k]);
+                        post_vec8_x2(r4, y, cb, pb, o, rf);
 #pragma unroll
-                    for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(rb + r_swz(hb, t, j, ch, jmajor)) = o[j];
-                    const int h = h0 + v * kVec;
-                    if (valid_t && h < H) {
-                        const int64_t base = (t0 + t) * kHC * (int64_t)H + h;
+                        for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(rp + j * lay.s_j) = o[j];
+                        if (t0 + t < T) {
+                            uint16_t *dst = rrow + p_goff[k];
 #pragma unroll
-                        for (int i = 0; i < kHC; ++i) st_stream(R_out + base + (int64_t)i * H, o[i]);
+                            for (int i = 0; i < kHC; ++i) st_stream(dst + (int64_t)i * H, o[i]);
+                        }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&postd[b]);
             }
         }
-    } else if (warp < kWCB) {
-        // ================================ projection + Gram partials, records
+    } else if (warp < kWP2 + kP2) {
+        // ================================ projection + Gram partials of this warp's blocks, records
         const int p = warp - kWP2, pt = tid - kWP2 * 32;
+        const int nb = nblk(p), bstart = blk0(p);
         const int gid = lane >> 2, tig = lane & 3;
-        const uint32_t tq = tbase + ((uint32_t)(32 * p) << 16);
-        // ldmatrix.x4 lane address: matrices (stream i0, k 0-7), (i0+1, k 0-7), (i0, k 8-15), (i0+1, k 8-15),
-        // row = token lane & 7
-        const int lj = (lane >> 3) & 1, lt = lane & 7, lk = 8 * (lane >> 4);
+        // Two ldmatrix.x4 orders over the 8 tokens (row = token lane & 7) of streams (i0, i0+1):
+        //   B order: (i0, k 0-7) (i0, k 8-15) (i0+1, k 0-7) (i0+1, k 8-15): registers {0,1} and {2,3}
+        //            are the B fragments of streams i0 and i0+1 as they stand;
+        //   A order: (i0, k 0-7) (i0+1, k 0-7) (i0, k 8-15) (i0+1, k 8-15): the four registers are the
+        //            A fragment of the 16 rows (stream i0 tokens, stream i0+1 tokens).
+        // Loading both keeps every MMA operand in the register order the instruction takes.
+        // Streams (2, 3) are 2 * s_j bytes further.
+        const int lt = lane & 7;
+        const int bj = lane >> 4, bk = 8 * ((lane >> 3) & 1);  // B order: stream offset, k offset
+        const int aj = (lane >> 3) & 1, ak = 8 * (lane >> 4);  // A order
+        auto lds_off = [&](int i, int j, int k) {
+            const int h = 16 * (bstart + i) + k;
+            return r_swz(h >> 6, lt, j, (h & 63) >> 3, lay);
+        };
+        const uint32_t s2j = 2u * (uint32_t)lay.s_j;
         // the lanes holding a diagonal (token == token) entry of the Gram tiles: token gid, when gid/2 == tig
         const bool gdiag = (gid >> 1) == tig;
         const int gsel = gid & 1;
+        uint64_t *rdy = kPost ? postd : full;
         for (int q = 0; q < n_it; ++q) {
             const int b = q % kNBuf;
             bwait(&rdy[b], (uint32_t)((q / kNBuf) & 1), dead);
             const uint32_t rb32 = smem_u32(smem + L.r_off(b));
-            float acc[3][4], gd[5][4];
-#pragma unroll
-            for (int mt = 0; mt < 3; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-#pragma unroll
-            for (int g = 0; g < 5; ++g)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) gd[g][e] = 0.f;
-            int hh = 16 * p * nHB + lk;  // this lane's hidden offset within the slice
-            for (int lb = 0; lb < nHB; ++lb, hh += 16) {
-                const int hb = hh >> 6, ch = (hh & 63) >> 3;
-                uint32_t f[4], g[4];
-                ldmatrix_x4(rb32 + r_swz(hb, lt, lj, ch, jmajor), f);      // streams 0, 1
-                ldmatrix_x4(rb32 + r_swz(hb, lt, 2 + lj, ch, jmajor), g);  // streams 2, 3
-                // Gram tiles: A rows are (stream x, token) for m < 8 and (stream y, token) for
-                // m >= 8, B columns (stream j, token); 5 MMAs cover the 10 distinct pairs:
-                // (0,2|0) (1,3|1) (2,1|2) (3,2|3) (1,3|0)
-                mma_bf16(gd[0], f[0], g[0], f[2], g[2], f[0], f[2]);
-                mma_bf16(gd[1], f[1], g[1], f[3], g[3], f[1], f[3]);
-                mma_bf16(gd[2], g[0], f[1], g[2], f[3], g[0], g[2]);
-                mma_bf16(gd[3], g[1], g[0], g[3], g[2], g[1], g[3]);
-                mma_bf16(gd[4], f[1], g[1], f[3], g[3], f[0], f[2]);
-                // projection: k16 steps of streams 0-3 at these 16 hidden values
-#pragma unroll
-                for (int jp = 0; jp < kHC; jp += 2) {
-                    uint32_t a[24];
-                    tmem_ld12(tq + (uint32_t)((lb * 4 + jp) * 16), a);
-                    tmem_ld12(tq + (uint32_t)((lb * 4 + jp + 1) * 16), a + 12);
-                    tmem_wait_ld();
-                    const uint32_t b00 = jp ? g[0] : f[0], b01 = jp ? g[2] : f[2];
-                    const uint32_t b10 = jp ? g[1] : f[1], b11 = jp ? g[3] : f[3];
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], b00, b01);
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], b10, b11);
-                }
-            }
-            // partials of this warp: [token][24 logits (hi + lo rows), 10 Gram entries, 2 pad]
             float *pw = sPart + ((size_t)((q & 1) * kP2 + p) * kG) * kRec;
+            {
+                // Gram tiles D = A x B with A rows (stream i0 | i0+1, token) and B columns (stream j,
+                // token): tiles (0,1|0) (0,1|1) (0,1|2) (0,1|3) (2,3|2) (2,3|3) cover the 10 distinct pairs
+                float gd[6][4];
+                auto gblock = [&](auto first_tag, int i) {
+                    constexpr bool kF = decltype(first_tag)::value;
+                    const uint32_t oB = lds_off(i, bj, bk), oA = lds_off(i, aj, ak);
+                    uint32_t f[4], g[4], fa[4], ga[4];
+                    ldmatrix_x4(rb32 + oB, f);
+                    ldmatrix_x4(rb32 + oB + s2j, g);
+                    ldmatrix_x4(rb32 + oA, fa);
+                    ldmatrix_x4(rb32 + oA + s2j, ga);
+                    mma_acc<kF>(gd[0], fa[0], fa[1], fa[2], fa[3], f[0], f[1]);
+                    mma_acc<kF>(gd[1], fa[0], fa[1], fa[2], fa[3], f[2], f[3]);
+                    mma_acc<kF>(gd[2], fa[0], fa[1], fa[2], fa[3], g[0], g[1]);
+                    mma_acc<kF>(gd[3], fa[0], fa[1], fa[2], fa[3], g[2], g[3]);
+                    mma_acc<kF>(gd[4], ga[0], ga[1], ga[2], ga[3], g[0], g[1]);
+                    mma_acc<kF>(gd[5], ga[0], ga[1], ga[2], ga[3], g[2], g[3]);
+                };
+                if (nb > 0) {
+                    gblock(std::true_type{}, 0);
+                    for (int i = 1; i < nb; ++i) gblock(std::false_type{}, i);
+                } else {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = 2 * tig + e;
-                pw[t * kRec + gid] = acc[0][e] + acc[1][2 + e];
-                pw[t * kRec + gid + 8] = acc[0][2 + e] + acc[2][e];
-                pw[t * kRec + gid + 16] = acc[1][e] + acc[2][2 + e];
-            }
-            if (gdiag) {
-                // D[m][n]: rows m < 8 are stream x of token m, rows m >= 8 stream y; this lane
-                // holds rows gid and gid + 8 at column gid
-                float u[5], w[5];
+                    for (int k = 0; k < 6; ++k)
 #pragma unroll
-                for (int k = 0; k < 5; ++k) {
-                    u[k] = gsel ? gd[k][1] : gd[k][0];
-                    w[k] = gsel ? gd[k][3] : gd[k][2];
+                        for (int e = 0; e < 4; ++e) gd[k][e] = 0.f;
                 }
-                float *gq = pw + gid * kRec + kNumMix;
-                // order (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-                gq[0] = u[0]; gq[1] = u[1]; gq[2] = u[2]; gq[3] = u[3];
-                gq[4] = u[4]; gq[5] = w[0]; gq[6] = w[4]; gq[7] = w[2]; gq[8] = w[1]; gq[9] = w[3];
-                gq[10] = 0.f; gq[11] = 0.f;
+                if (gdiag) {
+                    // D[m][n]: rows m < 8 are stream i0 of token m, rows m >= 8 stream i0+1; this lane
+                    // holds rows gid and gid + 8 at column gid
+                    float u[6], w[6];
+#pragma unroll
+                    for (int k = 0; k < 6; ++k) {
+                        u[k] = gsel ? gd[k][1] : gd[k][0];
+                        w[k] = gsel ? gd[k][3] : gd[k][2];
+                    }
+                    float *gq = pw + gid * kRec + kNumMix;
+                    // order (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                    gq[0] = u[0]; gq[1] = w[1]; gq[2] = u[4]; gq[3] = w[5];
+                    gq[4] = u[1]; gq[5] = u[2]; gq[6] = u[3]; gq[7] = w[2]; gq[8] = w[3]; gq[9] = u[5];
+                    gq[10] = 0.f; gq[11] = 0.f;
+                }
+            }
+            {
+                // projection: per block, the k16 steps of streams 0-3 (phi^T fragments from tensor
+                // memory, B = R' in the B order)
+                float acc[3][4];
+                auto pblock = [&](auto first_tag, int i) {
+                    constexpr bool kF = decltype(first_tag)::value;
+                    const uint32_t oB = lds_off(i, bj, bk);
+                    uint32_t f[4], g[4];
+                    ldmatrix_x4(rb32 + oB, f);
+                    ldmatrix_x4(rb32 + oB + s2j, g);
+                    uint32_t a[24];
+                    tmem_ld12(tq + (uint32_t)((i * 4) * 16), a);
+                    tmem_ld12(tq + (uint32_t)((i * 4 + 1) * 16), a + 12);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+                        mma_acc<kF>(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], f[0], f[1]);
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+                        mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], f[2], f[3]);
+                    tmem_ld12(tq + (uint32_t)((i * 4 + 2) * 16), a);
+                    tmem_ld12(tq + (uint32_t)((i * 4 + 3) * 16), a + 12);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+                        mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], g[0], g[1]);
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+                        mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], g[2], g[3]);
+                };
+                if (nb > 0) {
+                    pblock(std::true_type{}, 0);
+                    for (int i = 1; i < nb; ++i) pblock(std::false_type{}, i);
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+                }
+                // partial logits of this warp: [token][24 (hi + lo rows)]
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 2 * tig + e;
+                    pw[t * kRec + gid] = acc[0][e] + acc[1][2 + e];
+                    pw[t * kRec + gid + 8] = acc[0][2 + e] + acc[2][e];
+                    pw[t * kRec + gid + 16] = acc[1][e] + acc[2][2 + e];
+                }
             }
             named_sync(2, kP2 * 32);
             if (pt < kG * (kRec / 4)) {
-                // chunk qq of token t: sum of the warps' partials, sent to the owner's record slot
+                // chunk qq of token t: sum of the warps' partials (fixed order), sent to the owner's
+                // record slot
                 const int t = pt / (kRec / 4), qq = pt % (kRec / 4);
                 float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -419,12 +477,25 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                                                    __float_as_uint(s.z), __float_as_uint(s.w)));
             }
         }
-    } else if (warp < kWOwner) {
+    } else if (warp >= kWCB && warp < kWCB + kCB) {
         // ================================ combine + RMSNorm
         const int ct = tid - kWCB * 32;
         constexpr int kStride = kCB * 32;
-        // this thread's first item (token, vector) and the per-step advance, without divisions in the loop
-        const int t_first = ct / nvec, v_first = ct % nvec, dt = kStride / nvec, dv = kStride % nvec;
+        uint64_t *rdy = kPost ? postd : full;
+        // this thread's items (token, vector) item = ct + k * 128, the same in every group: shared
+        // memory offset of stream 0, token, X offset within the group's rows, RMSNorm weight offset
+        uint32_t c_roff[kCItems];
+        int c_t[kCItems], c_xoff[kCItems], c_v[kCItems];
+#pragma unroll
+        for (int k = 0; k < kCItems; ++k) {
+            const int item = ct + k * kStride;
+            const int t = item / nvec, v = item % nvec;
+            const bool on = item < kG * nvec && h0 + v * kVec < H;
+            c_t[k] = on ? t : kG;  // kG: no item
+            c_v[k] = v;
+            c_roff[k] = r_swz(v >> 3, t, 0, v & 7, lay);
+            c_xoff[k] = t * H + h0 + v * kVec;
+        }
         for (int q = 0; q < n_it; ++q) {
             const int b = q % kNBuf, s = q % kNPre;
             bwait(&rdy[b], (uint32_t)((q / kNBuf) & 1), dead);
@@ -432,31 +503,64 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             if (ct == 0 && q + kNPre < n_it) mbar_arrive_expect_tx(&pre_full[s], kG * 32);
             const int64_t t0 = group_t0(q);
             const unsigned char *rb = smem + L.r_off(b);
-            int t = t_first, v = v_first;
-            while (t < kG) {
-                const int h = h0 + v * kVec;
-                if (t0 + t < T && h < H) {
-                    const float4 pr = *reinterpret_cast<const float4 *>(sPreIn + ((size_t)s * kG + t) * 8);
-                    const float rstd = sPreIn[((size_t)s * kG + t) * 8 + 4];
+            const float *pin = sPreIn + (size_t)s * kG * 8;
+            uint16_t *xrow = X_out + t0 * (int64_t)H;
+#pragma unroll
+            for (int k = 0; k < kCItems; ++k) {
+                const int t = c_t[k];
+                if (t < kG && t0 + t < T) {
+                    const float4 pr = *reinterpret_cast<const float4 *>(pin + t * 8);
+                    const float rstd = pin[t * 8 + 4];
                     const float pre[kHC] = {pr.x, pr.y, pr.z, pr.w};
+                    const unsigned char *rp = rb + c_roff[k];
                     float rf[kHC][8], x[8];
 #pragma unroll
-                    for (int j = 0; j < kHC; ++j)
-                        unpack8(*reinterpret_cast<const uint4 *>(rb + r_swz(v >> 3, t, j, v & 7, jmajor)), rf[j]);
+                    for (int j = 0; j < kHC; ++j) unpack8(*reinterpret_cast<const uint4 *>(rp + j * lay.s_j), rf[j]);
                     combine_vec8_x2(rf, pre, x);
-                    st_stream(X_out + (t0 + t) * (int64_t)H + h,
-                              norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + v * 16)));
+                    st_stream(xrow + c_xoff[k], norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16)));
                 }
-                t += dt;
-                v += dv;
-                if (v >= nvec) { v -= nvec; ++t; }
             }
             fence_proxy_async_smem();  // the slot is refilled by TMA after this
             __syncwarp();
             if (lane == 0) mbar_arrive(&freeb[b]);
         }
+    } else if (warp == kWProd) {
+        // ================================ producer: tensor copies of group q into ring slot q % kNBuf
+        if (lane == 0) {
+            const uint32_t expect_bytes = (uint32_t)nHB * (4096 + (kPost ? 1024 : 0)) + (kPost ? 512 + 128 : 0);
+            int issued = 0;
+            for (int q = 0; q < n_it && !dead; ++q) {
+                const int b = q % kNBuf;
+                if (q >= kNBuf) bwait(&freeb[b], (uint32_t)((q / kNBuf - 1) & 1), dead);
+                if (dead) break;
+                const int t0 = (int)group_t0(q);
+                mbar_arrive_expect_tx(&full[b], expect_bytes);
+                if (lay.one_box) {
+                    tma_load_4d(smem + L.r_off(b), &maps.R, 0, t0, h0 / 64, 0, &full[b]);
+                    if (kPost) tma_load_3d(smem + L.y_off(b), &maps.Y, 0, t0, h0 / 64, &full[b]);
+                } else {
+                    for (int hb = 0; hb < nHB; ++hb) {
+                        tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
+                        if (kPost) tma_load_2d(smem + L.y_off(b) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &full[b]);
+                    }
+                }
+                if (kPost) {
+                    tma_load_2d(smem + L.comb_off(b), &maps.comb, 0, t0, &full[b]);
+                    tma_load_2d(smem + L.post_off(b), &maps.post, 0, t0, &full[b]);
+                }
+                ++issued;
+            }
+            // the copies of the last groups issued have landed (already true unless a wait timed out)
+            bool drained = false;
+            for (int q = issued > kNBuf ? issued - kNBuf : 0; q < issued; ++q)
+                mbar_wait_timed(&full[q % kNBuf], (uint32_t)((q / kNBuf) & 1), drained, kWaitLimitNs);
+            dead = dead || drained;
+        }
+        __syncwarp();
     } else {
         // ================================ owner
+        const float a_pre = mix_scales[0], a_post = mix_scales[1];
+        const float bl = lane < kNumMix ? bias[lane] : 0.f;
         for (int k = 0; k < nown; ++k) {
             const int q = first_owned + 2 * k, slot = k & 1;
             const int g = c - 8 * (q & 1);
@@ -467,6 +571,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             // floats 32-33 (Gram entries 8 and 9)
             const float *rv = sRecv + (size_t)slot * kC * kRec;
             float a = 0.f, a2 = 0.f;
+#pragma unroll
             for (int src = 0; src < kC; ++src) {
                 a += rv[src * kRec + lane];
                 if (lane < 2) a2 += rv[src * kRec + 32 + lane];
@@ -481,7 +586,8 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             const float ss = (G[0] + G[1]) + (G[2] + G[3]);
             const float r = 1.f / sqrtf(ss / (float)(kHC * H) + sc.hc_norm_eps);
             const float z = r * a;
-            const float pv = pre_head(z, bias, mix_scales);
+            // pre head (lanes 0-3)
+            const float pv = lane < 4 ? 1.f / (1.f + expf(-(a_pre * z + bl))) : 0.f;
             float pre[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) pre[i] = __shfl_sync(0xffffffffu, pv, i);
@@ -504,7 +610,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 const int64_t t = t0 + g;
                 if (lane < 4) pre_out[t * 4 + lane] = pv;
                 else if (lane < 8)
-                    post_out[t * 4 + lane - 4] = sc.hc_post_scale / (1.f + expf(-(mix_scales[1] * z + bias[lane])));
+                    post_out[t * 4 + lane - 4] = sc.hc_post_scale / (1.f + expf(-(a_post * z + bl)));
                 else if (lane < kNumMix) zstash[t * 16 + lane - 8] = z;  // residual-mix logits, normalised at the end
             }
         }
@@ -536,7 +642,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     if (any_dead && lane == 0) atomicOr(status, 1u);
     tmem_fence_before();
     __syncthreads();
-    if (warp == kWProd) tmem_dealloc(tbase, kTmemCols);
+    if (warp == kWOwner) tmem_dealloc(tbase, kTmemCols);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -576,8 +682,9 @@ int ws_slice(int H) { return ((H + 64 * kC - 1) / (64 * kC)) * 64; }
 
 bool ws_supported(int H) {
     const int Hs = ws_slice(H);
-    // tensor memory: Hs/64 hidden blocks x 4 streams x 16 columns per projection warp
-    return Hs <= kTmemCols && Hs / kVec <= 64 && Layout{Hs / 64}.bytes() + 1024 <= 227 * 1024;
+    // at most four 16-wide blocks per projection warp (so at most 8 blocks, 512 tensor-memory
+    // columns, per lane quadrant)
+    return Hs / 16 <= kMaxB16 && Layout{Hs / 64}.bytes() + 1024 <= 227 * 1024;
 }
 
 size_t ws_pack_bytes(int H) {
@@ -597,27 +704,41 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     WsMaps maps;
     std::memset(&maps, 0, sizeof maps);
     const cuuint64_t H = (cuuint64_t)a.H, T = (cuuint64_t)a.T;
-    bool jmajor = true;
-    {   // R [T][4][H] bf16 as (h, t, j) (box 64 x 8 x 4, stream-major rows in shared memory);
-        // if the encoder refuses the non-monotonic strides, as (h, j, t) (box 64 x 4 x 8)
+    const int nHB = Hs / 64;
+    RLayout lay{1024, nHB * 1024, true};
+    // R [T][4][H] bf16 as (h % 64, t, h / 64, j), one box {64, 8, nHB, 4} per group, and Y [T][H]
+    // as (h % 64, t, h / 64), one box {64, 8, nHB}: needs H % 64 == 0 (otherwise a block would run
+    // into the next row instead of the zero fill)
+    if (a.H % 64 != 0) lay.one_box = false;
+    if (lay.one_box) {
+        const cuuint64_t dims[4] = {64, T, H / 64, 4}, strides[3] = {H * 8, 128, H * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)kG, (cuuint32_t)nHB, 4};
+        lay.one_box = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.R, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess;
+    }
+    if (lay.one_box && post) {
+        const cuuint64_t dims[3] = {64, T, H / 64}, strides[2] = {H * 2, 128};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kG, (cuuint32_t)nHB};
+        lay.one_box = encode(fn, &maps.Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Y, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess;
+    }
+    if (!lay.one_box) {
+        // per 64-wide block: R as (h, t, j), box {64, 8, 4}; Y as (h, t), box {64, 8}
+        lay = RLayout{4096, 1024, false};
         const cuuint64_t dims[3] = {H, T, 4}, strides[2] = {H * 8, H * 2};
         const cuuint32_t box[3] = {64, (cuuint32_t)kG, 4};
-        if (encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess) {
-            jmajor = false;
-            const cuuint64_t dims2[3] = {H, 4, T}, strides2[2] = {H * 2, H * 8};
-            const cuuint32_t box2[3] = {64, 4, (cuuint32_t)kG};
-            if ((e = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims2, strides2, box2,
+        if ((e = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        if (post) {
+            const cuuint64_t dy[2] = {H, T}, sy[1] = {H * 2};
+            const cuuint32_t by[2] = {64, (cuuint32_t)kG};
+            if ((e = encode(fn, &maps.Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y, dy, sy, by,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
                 return e;
         }
     }
     if (post) {
-        const cuuint64_t dy[2] = {H, T}, sy[1] = {H * 2};
-        const cuuint32_t by[2] = {64, (cuuint32_t)kG};
-        if ((e = encode(fn, &maps.Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y, dy, sy, by, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-            cudaSuccess)
-            return e;
         const cuuint64_t dc[2] = {16, T}, scm[1] = {64};
         const cuuint32_t bc[2] = {16, (cuuint32_t)kG};
         if ((e = encode(fn, &maps.comb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.prev_comb, dc, scm, bc,
@@ -671,7 +792,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
     return cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                              a.H, Hs, jmajor, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status);
+                              a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status);
 }
 
 }  // namespace mhc

@@ -41,6 +41,37 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, bool &
         if (mbar_try_wait(bar, parity)) return;
     dead = true;
 }
+// As mbar_try_wait, but an incomplete phase may suspend the thread for up to
+// hint_ns nanoseconds (it resumes earlier when the phase completes), so a
+// waiting warp takes far fewer issue slots than with back-to-back polls.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait bounded in time: gives up (sets `dead`) once limit_ns of global time
+// have passed; after one timeout, later waits make a single test.
+__device__ __forceinline__ void mbar_wait_timed(uint64_t *bar, uint32_t parity, bool &dead, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity) || dead) return;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_hint(bar, parity, 1000u)) return;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            dead = true;
+            return;
+        }
+    }
+}
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
@@ -61,6 +92,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];\n" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
         : "memory");
 }
 
