@@ -73,8 +73,8 @@ constexpr int kP2 = 7;
 constexpr int kWOwner = kWP2 + kP2;       // owner warp (14)
 constexpr int kWCB = kWOwner + 1;         // combine warps 15-18
 constexpr int kCB = 4;
-constexpr int kWProd = kWCB + kCB;        // producer warp (19)
-constexpr int kNT = (kWProd + 1) * 32;
+constexpr int kWSend = kWCB + kCB;        // sender warp (19): sums the projection partials, sends records
+constexpr int kNT = (kWSend + 1) * 32;
 constexpr int kMaxB16 = 4 * kP2;          // 16-wide hidden blocks per slice: at most four per projection warp
 constexpr int kP1Items = (kG * kMaxB16 * 2 + kP1 * 32 - 1) / (kP1 * 32);  // post items per thread
 constexpr int kCItems = (kG * kMaxB16 * 2 + kCB * 32 - 1) / (kCB * 32);   // combine items per thread
@@ -151,8 +151,8 @@ struct Layout {
     __host__ __device__ size_t prein_off() const { return recv_off() + (size_t)2 * kC * kRec * 4; }     // [kNPre][8][8]
     __host__ __device__ size_t gam_off() const { return prein_off() + (size_t)kNPre * kG * 8 * 4; }     // [Hs] bf16
     __host__ __device__ size_t bar_off() const { return gam_off() + (size_t)nHB * 64 * 2; }
-    // full[kNBuf], postd[kNBuf], freeb[kNBuf], part_full[2], pre_full[kNPre]
-    static constexpr int kBars = 3 * kNBuf + 2 + kNPre;
+    // full[kNBuf], postd[kNBuf], part_full[2], pre_full[kNPre], parts_ready[2], parts_free[2]
+    static constexpr int kBars = 2 * kNBuf + 2 + kNPre + 4;
     __host__ __device__ size_t tmem_off() const { return bar_off() + (size_t)kBars * 8; }
     __host__ __device__ size_t bytes() const { return tmem_off() + 8; }
 };
@@ -201,8 +201,8 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     float *sPreIn = reinterpret_cast<float *>(smem + L.prein_off());
     unsigned char *sGam = smem + L.gam_off();
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off());
-    uint64_t *full = bars, *postd = bars + kNBuf, *freeb = bars + 2 * kNBuf, *part_full = bars + 3 * kNBuf,
-             *pre_full = bars + 3 * kNBuf + 2;
+    uint64_t *full = bars, *postd = bars + kNBuf, *part_full = bars + 2 * kNBuf, *pre_full = bars + 2 * kNBuf + 2,
+             *parts_ready = pre_full + kNPre, *parts_free = parts_ready + 2;
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.tmem_off());
 
     const int h0 = c * Hs;
@@ -227,9 +227,12 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             for (int i = 0; i < kNBuf; ++i) {
                 mbar_init(&full[i], 1);
                 mbar_init(&postd[i], kP1);
-                mbar_init(&freeb[i], kCB);
             }
-            for (int i = 0; i < 2; ++i) mbar_init(&part_full[i], 1);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&part_full[i], 1);
+                mbar_init(&parts_ready[i], kP2);
+                mbar_init(&parts_free[i], 1);
+            }
             for (int i = 0; i < kNPre; ++i) mbar_init(&pre_full[i], 1);
             fence_mbar_init();
         }
@@ -336,19 +339,15 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         }
     } else if (warp < kWP2 + kP2) {
         // ================================ projection + Gram partials of this warp's blocks, records
-        const int p = warp - kWP2, pt = tid - kWP2 * 32;
+        const int p = warp - kWP2;
         const int nb = nblk(p), bstart = blk0(p);
         const int gid = lane >> 2, tig = lane & 3;
-        // Two ldmatrix.x4 orders over the 8 tokens (row = token lane & 7) of streams (i0, i0+1):
-        //   B order: (i0, k 0-7) (i0, k 8-15) (i0+1, k 0-7) (i0+1, k 8-15): registers {0,1} and {2,3}
-        //            are the B fragments of streams i0 and i0+1 as they stand;
-        //   A order: (i0, k 0-7) (i0+1, k 0-7) (i0, k 8-15) (i0+1, k 8-15): the four registers are the
-        //            A fragment of the 16 rows (stream i0 tokens, stream i0+1 tokens).
-        // Loading both keeps every MMA operand in the register order the instruction takes.
-        // Streams (2, 3) are 2 * s_j bytes further.
+        // ldmatrix.x4 over the 8 tokens (row = token lane & 7) of streams (i0, i0+1) in the order
+        // (i0, k 0-7) (i0, k 8-15) (i0+1, k 0-7) (i0+1, k 8-15): registers {0,1} and {2,3} are the B
+        // fragments of streams i0 and i0+1, and {0,2,1,3} the A fragment of the 16 rows (stream i0
+        // tokens, stream i0+1 tokens).  Streams (2, 3) are 2 * s_j bytes further.
         const int lt = lane & 7;
-        const int bj = lane >> 4, bk = 8 * ((lane >> 3) & 1);  // B order: stream offset, k offset
-        const int aj = (lane >> 3) & 1, ak = 8 * (lane >> 4);  // A order
+        const int bj = lane >> 4, bk = 8 * ((lane >> 3) & 1);  // stream offset, k offset
         auto lds_off = [&](int i, int j, int k) {
             const int h = 16 * (bstart + i) + k;
             return r_swz(h >> 6, lt, j, (h & 63) >> 3, lay);
@@ -363,24 +362,26 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             bwait(&rdy[b], (uint32_t)((q / kNBuf) & 1), dead);
             const uint32_t rb32 = smem_u32(smem + L.r_off(b));
             float *pw = sPart + ((size_t)((q & 1) * kP2 + p) * kG) * kRec;
+            // the sender has read this partial slot's previous group (q - 2)
+            if (q >= 2) bwait(&parts_free[q & 1], (uint32_t)(((q - 2) >> 1) & 1), dead);
             {
                 // Gram tiles D = A x B with A rows (stream i0 | i0+1, token) and B columns (stream j,
                 // token): tiles (0,1|0) (0,1|1) (0,1|2) (0,1|3) (2,3|2) (2,3|3) cover the 10 distinct pairs
                 float gd[6][4];
                 auto gblock = [&](auto first_tag, int i) {
                     constexpr bool kF = decltype(first_tag)::value;
-                    const uint32_t oB = lds_off(i, bj, bk), oA = lds_off(i, aj, ak);
-                    uint32_t f[4], g[4], fa[4], ga[4];
+                    const uint32_t oB = lds_off(i, bj, bk);
+                    uint32_t f[4], g[4];
                     ldmatrix_x4(rb32 + oB, f);
                     ldmatrix_x4(rb32 + oB + s2j, g);
-                    ldmatrix_x4(rb32 + oA, fa);
-                    ldmatrix_x4(rb32 + oA + s2j, ga);
-                    mma_acc<kF>(gd[0], fa[0], fa[1], fa[2], fa[3], f[0], f[1]);
-                    mma_acc<kF>(gd[1], fa[0], fa[1], fa[2], fa[3], f[2], f[3]);
-                    mma_acc<kF>(gd[2], fa[0], fa[1], fa[2], fa[3], g[0], g[1]);
-                    mma_acc<kF>(gd[3], fa[0], fa[1], fa[2], fa[3], g[2], g[3]);
-                    mma_acc<kF>(gd[4], ga[0], ga[1], ga[2], ga[3], g[0], g[1]);
-                    mma_acc<kF>(gd[5], ga[0], ga[1], ga[2], ga[3], g[2], g[3]);
+                    // the A-order fragment of streams (i0, i0+1) is the B-order load permuted:
+                    // (i0 k0-7, i0+1 k0-7, i0 k8-15, i0+1 k8-15) = (f0, f2, f1, f3)
+                    mma_acc<kF>(gd[0], f[0], f[2], f[1], f[3], f[0], f[1]);
+                    mma_acc<kF>(gd[1], f[0], f[2], f[1], f[3], f[2], f[3]);
+                    mma_acc<kF>(gd[2], f[0], f[2], f[1], f[3], g[0], g[1]);
+                    mma_acc<kF>(gd[3], f[0], f[2], f[1], f[3], g[2], g[3]);
+                    mma_acc<kF>(gd[4], g[0], g[2], g[1], g[3], g[0], g[1]);
+                    mma_acc<kF>(gd[5], g[0], g[2], g[1], g[3], g[2], g[3]);
                 };
                 if (nb > 0) {
                     gblock(std::true_type{}, 0);
@@ -455,33 +456,41 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                     pw[t * kRec + gid + 16] = acc[1][e] + acc[2][2 + e];
                 }
             }
-            named_sync(2, kP2 * 32);
-            if (pt < kG * (kRec / 4)) {
-                // chunk qq of token t: sum of the warps' partials (fixed order), sent to the owner's
-                // record slot
-                const int t = pt / (kRec / 4), qq = pt % (kRec / 4);
-                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w2 = 0; w2 < kP2; ++w2) {
-                    const float4 x = *reinterpret_cast<const float4 *>(
-                        sPart + ((size_t)((q & 1) * kP2 + w2) * kG + t) * kRec + 4 * qq);
-                    s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-                }
-                // the owner has read its slot for group q-4 once (pre, rstd) of q-4 arrived
-                if (q >= 4) bwait(&pre_full[(q - 4) % kNPre], (uint32_t)(((q - 4) / kNPre) & 1), dead);
-                const uint32_t owner = (uint32_t)((t + 8 * (q & 1)) % kC);
-                const int slot = (q >> 1) & 1;
-                const uint32_t raddr = mapa(smem_u32(sRecv + ((size_t)slot * kC + c) * kRec + 4 * qq), owner);
-                const uint32_t rbar = mapa(smem_u32(&part_full[slot]), owner);
-                st_async16(raddr, rbar, make_uint4(__float_as_uint(s.x), __float_as_uint(s.y),
-                                                   __float_as_uint(s.z), __float_as_uint(s.w)));
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&parts_ready[q & 1]);
         }
     } else if (warp >= kWCB && warp < kWCB + kCB) {
         // ================================ combine + RMSNorm
-        const int ct = tid - kWCB * 32;
+        const int ct = tid - kWCB * 32, cw = warp - kWCB;
         constexpr int kStride = kCB * 32;
         uint64_t *rdy = kPost ? postd : full;
+        // Tensor copies of group q into ring slot q % kNBuf, shared by the four combine warps (one per
+        // SM sub-partition) so that no sub-partition's issue stalls behind all of them: warp cw copies
+        // R stream cw (one box, or the 64-wide blocks hb = cw mod 4 of the per-block layout), the Y
+        // blocks hb = cw mod 4, and warp 0 (1) the previous comb (post) mixes.  Warp 0 sets the
+        // expected byte count.
+        const uint32_t expect_bytes = (uint32_t)nHB * (4096 + (kPost ? 1024 : 0)) + (kPost ? 512 + 128 : 0);
+        auto issue = [&](int q) {
+            const int b = q % kNBuf;
+            const int t0 = (int)group_t0(q);
+            if (cw == 0) mbar_arrive_expect_tx(&full[b], expect_bytes);
+            unsigned char *rs = smem + L.r_off(b);
+            if (lay.one_box) {
+                tma_load_4d(rs + cw * lay.s_j, &maps.R, 0, t0, h0 / 64, cw, &full[b]);
+                if (kPost)
+                    for (int hb = cw; hb < nHB; hb += kCB)
+                        tma_load_3d(smem + L.y_off(b) + hb * 1024, &maps.Y, 0, t0, h0 / 64 + hb, &full[b]);
+            } else {
+                for (int hb = cw; hb < nHB; hb += kCB) {
+                    tma_load_3d(rs + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
+                    if (kPost) tma_load_2d(smem + L.y_off(b) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &full[b]);
+                }
+            }
+            if (kPost && cw == 0) tma_load_2d(smem + L.comb_off(b), &maps.comb, 0, t0, &full[b]);
+            if (kPost && cw == 1) tma_load_2d(smem + L.post_off(b), &maps.post, 0, t0, &full[b]);
+        };
+        if (lane == 0)
+            for (int q = 0; q < kNBuf && q < n_it; ++q) issue(q);
         // this thread's items (token, vector) item = ct + k * 128, the same in every group: shared
         // memory offset of stream 0, token, X offset within the group's rows, RMSNorm weight offset
         uint32_t c_roff[kCItems];
@@ -520,47 +529,64 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                     st_stream(xrow + c_xoff[k], norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16)));
                 }
             }
-            fence_proxy_async_smem();  // the slot is refilled by TMA after this
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&freeb[b]);
+            // every use of the slot (post, projection, combine) is over: refill it with group q + kNBuf
+            fence_proxy_async_smem();
+            named_sync(3, kCB * 32);
+            if (lane == 0 && q + kNBuf < n_it && !dead) issue(q + kNBuf);
         }
-    } else if (warp == kWProd) {
-        // ================================ producer: tensor copies of group q into ring slot q % kNBuf
-        if (lane == 0) {
-            const uint32_t expect_bytes = (uint32_t)nHB * (4096 + (kPost ? 1024 : 0)) + (kPost ? 512 + 128 : 0);
-            int issued = 0;
-            for (int q = 0; q < n_it && !dead; ++q) {
-                const int b = q % kNBuf;
-                if (q >= kNBuf) bwait(&freeb[b], (uint32_t)((q / kNBuf - 1) & 1), dead);
-                if (dead) break;
-                const int t0 = (int)group_t0(q);
-                mbar_arrive_expect_tx(&full[b], expect_bytes);
-                if (lay.one_box) {
-                    tma_load_4d(smem + L.r_off(b), &maps.R, 0, t0, h0 / 64, 0, &full[b]);
-                    if (kPost) tma_load_3d(smem + L.y_off(b), &maps.Y, 0, t0, h0 / 64, &full[b]);
-                } else {
-                    for (int hb = 0; hb < nHB; ++hb) {
-                        tma_load_3d(smem + L.r_off(b) + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
-                        if (kPost) tma_load_2d(smem + L.y_off(b) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &full[b]);
-                    }
-                }
-                if (kPost) {
-                    tma_load_2d(smem + L.comb_off(b), &maps.comb, 0, t0, &full[b]);
-                    tma_load_2d(smem + L.post_off(b), &maps.post, 0, t0, &full[b]);
-                }
-                ++issued;
-            }
+        if (lane == 0 && cw == 0) {
             // the copies of the last groups issued have landed (already true unless a wait timed out)
             bool drained = false;
-            for (int q = issued > kNBuf ? issued - kNBuf : 0; q < issued; ++q)
+            for (int q = n_it > kNBuf ? n_it - kNBuf : 0; q < n_it; ++q)
                 mbar_wait_timed(&full[q % kNBuf], (uint32_t)((q / kNBuf) & 1), drained, kWaitLimitNs);
             dead = dead || drained;
         }
-        __syncwarp();
+    } else if (warp == kWSend) {
+        // ================================ sender: records of the group from the projection partials
+        for (int q = 0; q < n_it; ++q) {
+            bwait(&parts_ready[q & 1], (uint32_t)((q >> 1) & 1), dead);
+            // chunk (token t, 16-byte piece qq) = lane + 32 k: sum of the warps' partials, fixed order
+            float4 sum[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int ch = lane + 32 * k;
+                sum[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ch < kG * (kRec / 4)) {
+                    const int t = ch / (kRec / 4), qq = ch % (kRec / 4);
+#pragma unroll
+                    for (int w2 = 0; w2 < kP2; ++w2) {
+                        const float4 x = *reinterpret_cast<const float4 *>(
+                            sPart + ((size_t)((q & 1) * kP2 + w2) * kG + t) * kRec + 4 * qq);
+                        sum[k].x += x.x; sum[k].y += x.y; sum[k].z += x.z; sum[k].w += x.w;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&parts_free[q & 1]);
+            // the owner has read its record slot for group q-4 once (pre, rstd) of q-4 arrived
+            if (q >= 4) bwait(&pre_full[(q - 4) % kNPre], (uint32_t)(((q - 4) / kNPre) & 1), dead);
+            const int slot = (q >> 1) & 1;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int ch = lane + 32 * k;
+                if (ch < kG * (kRec / 4)) {
+                    const int t = ch / (kRec / 4), qq = ch % (kRec / 4);
+                    const uint32_t owner = (uint32_t)((t + 8 * (q & 1)) % kC);
+                    const uint32_t raddr = mapa(smem_u32(sRecv + ((size_t)slot * kC + c) * kRec + 4 * qq), owner);
+                    const uint32_t rbar = mapa(smem_u32(&part_full[slot]), owner);
+                    st_async16(raddr, rbar, make_uint4(__float_as_uint(sum[k].x), __float_as_uint(sum[k].y),
+                                                       __float_as_uint(sum[k].z), __float_as_uint(sum[k].w)));
+                }
+            }
+        }
     } else {
         // ================================ owner
         const float a_pre = mix_scales[0], a_post = mix_scales[1];
         const float bl = lane < kNumMix ? bias[lane] : 0.f;
+        // the reductions' mean and the reciprocal square roots use a reciprocal multiply and the
+        // correctly rounded rsqrt / rcp: within 1 ulp of the divide-based forms, and a shorter
+        // dependent chain on the path every CTA's combine waits for
+        const float inv_kh = 1.f / (float)(kHC * H), inv_h = 1.f / (float)H;
         for (int k = 0; k < nown; ++k) {
             const int q = first_owned + 2 * k, slot = k & 1;
             const int g = c - 8 * (q & 1);
@@ -584,10 +610,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             G[8] = __shfl_sync(0xffffffffu, a2, 0);
             G[9] = __shfl_sync(0xffffffffu, a2, 1);
             const float ss = (G[0] + G[1]) + (G[2] + G[3]);
-            const float r = 1.f / sqrtf(ss / (float)(kHC * H) + sc.hc_norm_eps);
+            const float r = __frsqrt_rn(ss * inv_kh + sc.hc_norm_eps);
             const float z = r * a;
             // pre head (lanes 0-3)
-            const float pv = lane < 4 ? 1.f / (1.f + expf(-(a_pre * z + bl))) : 0.f;
+            const float pv = lane < 4 ? __frcp_rn(1.f + expf(-(a_pre * z + bl))) : 0.f;
             float pre[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) pre[i] = __shfl_sync(0xffffffffu, pv, i);
@@ -596,7 +622,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                        pre[3] * pre[3] * G[3];
             sx += 2.f * (pre[0] * pre[1] * G[4] + pre[0] * pre[2] * G[5] + pre[0] * pre[3] * G[6] +
                          pre[1] * pre[2] * G[7] + pre[1] * pre[3] * G[8] + pre[2] * pre[3] * G[9]);
-            const float rstd = 1.f / sqrtf(fmaxf(sx, 0.f) / (float)H + sc.rmsnorm_eps);
+            const float rstd = __frsqrt_rn(fmaxf(sx, 0.f) * inv_h + sc.rmsnorm_eps);
             // (pre, rstd) to every CTA of the cluster: lane d < 16 sends to CTA d
             if (lane < kC) {
                 const int s = q % kNPre;
@@ -706,19 +732,19 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     const cuuint64_t H = (cuuint64_t)a.H, T = (cuuint64_t)a.T;
     const int nHB = Hs / 64;
     RLayout lay{1024, nHB * 1024, true};
-    // R [T][4][H] bf16 as (h % 64, t, h / 64, j), one box {64, 8, nHB, 4} per group, and Y [T][H]
-    // as (h % 64, t, h / 64), one box {64, 8, nHB}: needs H % 64 == 0 (otherwise a block would run
-    // into the next row instead of the zero fill)
+    // R [T][4][H] bf16 as (h % 64, t, h / 64, j), one box {64, 8, nHB, 1} per stream and group, and
+    // Y [T][H] as (h % 64, t, h / 64), one box {64, 8, 1} per 64-wide block: needs H % 64 == 0
+    // (otherwise a block would run into the next row instead of the zero fill)
     if (a.H % 64 != 0) lay.one_box = false;
     if (lay.one_box) {
         const cuuint64_t dims[4] = {64, T, H / 64, 4}, strides[3] = {H * 8, 128, H * 2};
-        const cuuint32_t box[4] = {64, (cuuint32_t)kG, (cuuint32_t)nHB, 4};
+        const cuuint32_t box[4] = {64, (cuuint32_t)kG, (cuuint32_t)nHB, 1};
         lay.one_box = encode(fn, &maps.R, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.R, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess;
     }
     if (lay.one_box && post) {
         const cuuint64_t dims[3] = {64, T, H / 64}, strides[2] = {H * 2, 128};
-        const cuuint32_t box[3] = {64, (cuuint32_t)kG, (cuuint32_t)nHB};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kG, 1};
         lay.one_box = encode(fn, &maps.Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Y, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess;
     }
