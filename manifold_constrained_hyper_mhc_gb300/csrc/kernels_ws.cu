@@ -364,97 +364,80 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             float *pw = sPart + ((size_t)((q & 1) * kP2 + p) * kG) * kRec;
             // the sender has read this partial slot's previous group (q - 2)
             if (q >= 2) bwait(&parts_free[q & 1], (uint32_t)(((q - 2) >> 1) & 1), dead);
-            {
-                // Gram tiles D = A x B with A rows (stream i0 | i0+1, token) and B columns (stream j,
-                // token): tiles (0,1|0) (0,1|1) (0,1|2) (0,1|3) (2,3|2) (2,3|3) cover the 10 distinct pairs
-                float gd[6][4];
-                auto gblock = [&](auto first_tag, int i) {
-                    constexpr bool kF = decltype(first_tag)::value;
-                    const uint32_t oB = lds_off(i, bj, bk);
-                    uint32_t f[4], g[4];
-                    ldmatrix_x4(rb32 + oB, f);
-                    ldmatrix_x4(rb32 + oB + s2j, g);
-                    // the A-order fragment of streams (i0, i0+1) is the B-order load permuted:
-                    // (i0 k0-7, i0+1 k0-7, i0 k8-15, i0+1 k8-15) = (f0, f2, f1, f3)
-                    mma_acc<kF>(gd[0], f[0], f[2], f[1], f[3], f[0], f[1]);
-                    mma_acc<kF>(gd[1], f[0], f[2], f[1], f[3], f[2], f[3]);
-                    mma_acc<kF>(gd[2], f[0], f[2], f[1], f[3], g[0], g[1]);
-                    mma_acc<kF>(gd[3], f[0], f[2], f[1], f[3], g[2], g[3]);
-                    mma_acc<kF>(gd[4], g[0], g[2], g[1], g[3], g[0], g[1]);
-                    mma_acc<kF>(gd[5], g[0], g[2], g[1], g[3], g[2], g[3]);
-                };
-                if (nb > 0) {
-                    gblock(std::true_type{}, 0);
-                    for (int i = 1; i < nb; ++i) gblock(std::false_type{}, i);
-                } else {
+            // per block: one ldmatrix.x4 per stream pair feeds the Gram tiles D = A x B (A rows
+            // (stream i0 | i0+1, token), B columns (stream j, token); tiles (0,1|0) (0,1|1) (0,1|2)
+            // (0,1|3) (2,3|2) (2,3|3) cover the 10 distinct pairs) and the projection's k16 steps of
+            // streams 0-3 (phi^T fragments from tensor memory, B = R')
+            float gd[6][4], acc[3][4];
+            auto block = [&](auto first_tag, int i) {
+                constexpr bool kF = decltype(first_tag)::value;
+                const uint32_t oB = lds_off(i, bj, bk);
+                uint32_t f[4], g[4];
+                ldmatrix_x4(rb32 + oB, f);
+                ldmatrix_x4(rb32 + oB + s2j, g);
+                uint32_t a[24];
+                tmem_ld12(tq + (uint32_t)((i * 4) * 16), a);
+                tmem_ld12(tq + (uint32_t)((i * 4 + 1) * 16), a + 12);
+                // the A-order fragment of streams (i0, i0+1) is the B-order load permuted:
+                // (i0 k0-7, i0+1 k0-7, i0 k8-15, i0+1 k8-15) = (f0, f2, f1, f3)
+                mma_acc<kF>(gd[0], f[0], f[2], f[1], f[3], f[0], f[1]);
+                mma_acc<kF>(gd[1], f[0], f[2], f[1], f[3], f[2], f[3]);
+                mma_acc<kF>(gd[2], f[0], f[2], f[1], f[3], g[0], g[1]);
+                mma_acc<kF>(gd[3], f[0], f[2], f[1], f[3], g[2], g[3]);
+                mma_acc<kF>(gd[4], g[0], g[2], g[1], g[3], g[0], g[1]);
+                mma_acc<kF>(gd[5], g[0], g[2], g[1], g[3], g[2], g[3]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 6; ++k)
+                for (int mt = 0; mt < 3; ++mt)
+                    mma_acc<kF>(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], f[0], f[1]);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) gd[k][e] = 0.f;
-                }
-                if (gdiag) {
-                    // D[m][n]: rows m < 8 are stream i0 of token m, rows m >= 8 stream i0+1; this lane
-                    // holds rows gid and gid + 8 at column gid
-                    float u[6], w[6];
+                for (int mt = 0; mt < 3; ++mt)
+                    mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], f[2], f[3]);
+                tmem_ld12(tq + (uint32_t)((i * 4 + 2) * 16), a);
+                tmem_ld12(tq + (uint32_t)((i * 4 + 3) * 16), a + 12);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 6; ++k) {
-                        u[k] = gsel ? gd[k][1] : gd[k][0];
-                        w[k] = gsel ? gd[k][3] : gd[k][2];
-                    }
-                    float *gq = pw + gid * kRec + kNumMix;
-                    // order (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-                    gq[0] = u[0]; gq[1] = w[1]; gq[2] = u[4]; gq[3] = w[5];
-                    gq[4] = u[1]; gq[5] = u[2]; gq[6] = u[3]; gq[7] = w[2]; gq[8] = w[3]; gq[9] = u[5];
-                    gq[10] = 0.f; gq[11] = 0.f;
-                }
+                for (int mt = 0; mt < 3; ++mt)
+                    mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], g[0], g[1]);
+#pragma unroll
+                for (int mt = 0; mt < 3; ++mt)
+                    mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], g[2], g[3]);
+            };
+            if (nb > 0) {
+                block(std::true_type{}, 0);
+                for (int i = 1; i < nb; ++i) block(std::false_type{}, i);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 6; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) gd[k][e] = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < 3; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
             }
-            {
-                // projection: per block, the k16 steps of streams 0-3 (phi^T fragments from tensor
-                // memory, B = R' in the B order)
-                float acc[3][4];
-                auto pblock = [&](auto first_tag, int i) {
-                    constexpr bool kF = decltype(first_tag)::value;
-                    const uint32_t oB = lds_off(i, bj, bk);
-                    uint32_t f[4], g[4];
-                    ldmatrix_x4(rb32 + oB, f);
-                    ldmatrix_x4(rb32 + oB + s2j, g);
-                    uint32_t a[24];
-                    tmem_ld12(tq + (uint32_t)((i * 4) * 16), a);
-                    tmem_ld12(tq + (uint32_t)((i * 4 + 1) * 16), a + 12);
-                    tmem_wait_ld();
+            if (gdiag) {
+                // D[m][n]: rows m < 8 are stream i0 of token m, rows m >= 8 stream i0+1; this lane
+                // holds rows gid and gid + 8 at column gid
+                float u[6], w[6];
 #pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_acc<kF>(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], f[0], f[1]);
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], f[2], f[3]);
-                    tmem_ld12(tq + (uint32_t)((i * 4 + 2) * 16), a);
-                    tmem_ld12(tq + (uint32_t)((i * 4 + 3) * 16), a + 12);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3], g[0], g[1]);
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-                        mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], g[2], g[3]);
-                };
-                if (nb > 0) {
-                    pblock(std::true_type{}, 0);
-                    for (int i = 1; i < nb; ++i) pblock(std::false_type{}, i);
-                } else {
-#pragma unroll
-                    for (int mt = 0; mt < 3; ++mt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+                for (int k = 0; k < 6; ++k) {
+                    u[k] = gsel ? gd[k][1] : gd[k][0];
+                    w[k] = gsel ? gd[k][3] : gd[k][2];
                 }
-                // partial logits of this warp: [token][24 (hi + lo rows)]
+                float *gq = pw + gid * kRec + kNumMix;
+                // order (0,0) (1,1) (2,2) (3,3) (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                gq[0] = u[0]; gq[1] = w[1]; gq[2] = u[4]; gq[3] = w[5];
+                gq[4] = u[1]; gq[5] = u[2]; gq[6] = u[3]; gq[7] = w[2]; gq[8] = w[3]; gq[9] = u[5];
+                gq[10] = 0.f; gq[11] = 0.f;
+            }
+            // partial logits of this warp: [token][24 (hi + lo rows)]
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 2 * tig + e;
-                    pw[t * kRec + gid] = acc[0][e] + acc[1][2 + e];
-                    pw[t * kRec + gid + 8] = acc[0][2 + e] + acc[2][e];
-                    pw[t * kRec + gid + 16] = acc[1][e] + acc[2][2 + e];
-                }
+            for (int e = 0; e < 2; ++e) {
+                const int t = 2 * tig + e;
+                pw[t * kRec + gid] = acc[0][e] + acc[1][2 + e];
+                pw[t * kRec + gid + 8] = acc[0][2 + e] + acc[2][e];
+                pw[t * kRec + gid + 16] = acc[1][e] + acc[2][2 + e];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&parts_ready[q & 1]);
