@@ -105,6 +105,22 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": float(np.nanmax([num(r[2]) for r in rows]))}
 
 
+def measured_traffic(schedule, workload, T, H):
+    """DRAM bytes (read + write) per launch of the dominant kernel from the committed ncu
+    capture in profiles/, or None when there is none for this schedule and workload or the
+    kernel source has changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{schedule}_{workload}_{T}x{H}.traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+            return None
+    return rec["dram_bytes_read"] + rec["dram_bytes_write"]
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
@@ -280,7 +296,7 @@ def run_ours(args, rank, world, lr, dist):
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
                    "hbm_gbs": achieved, "hbm_frac": achieved / peak},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": measured_traffic(sched, w.name, T, H), "peak_source": peak_src,
                      "kernel": f"whole call ({launches} launches), algorithmic bytes {abytes}"},
         "gpu_launches": launches * args.steps,
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
