@@ -689,7 +689,7 @@ cudaError_t get_encode(EncodeTiledFn &fn) {
 cudaError_t encode(EncodeTiledFn fn, CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr,
                    const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
                    CUtensorMapSwizzle swz) {
-    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};  // one per dimension, up to rank 5
     CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
