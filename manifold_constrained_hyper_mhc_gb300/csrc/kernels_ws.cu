@@ -78,8 +78,9 @@ constexpr int kNT = (kWSend + 1) * 32;
 constexpr int kMaxB16 = 4 * kP2;          // 16-wide hidden blocks per slice: at most four per projection warp
 constexpr int kP1Items = (kG * kMaxB16 * 2 + kP1 * 32 - 1) / (kP1 * 32);  // post items per thread
 constexpr int kCItems = (kG * kMaxB16 * 2 + kCB * 32 - 1) / (kCB * 32);   // combine items per thread
-constexpr int kNBuf = 5;                  // ring of R / Y / mix tiles
-constexpr int kNPre = 5;                  // (pre, rstd) slots; must be >= kNBuf
+constexpr int kNBuf = 6;                  // ring of R tiles (R' in place), refilled after the combine
+constexpr int kNY = 3;                    // ring of Y + previous-mix tiles, refilled after the projection
+constexpr int kNPre = 6;                  // (pre, rstd) slots; must be >= kNBuf
 constexpr int kRec = 36;                  // floats per record: 24 logits, 10 Gram entries, 2 pad
 constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
@@ -144,15 +145,15 @@ struct Layout {
     __host__ __device__ size_t ybuf() const { return (size_t)nHB * 1024; }
     __host__ __device__ size_t r_off(int b) const { return (size_t)b * rbuf(); }
     __host__ __device__ size_t y_off(int b) const { return kNBuf * rbuf() + (size_t)b * ybuf(); }
-    __host__ __device__ size_t comb_off(int b) const { return y_off(kNBuf) + (size_t)b * 512; }
-    __host__ __device__ size_t post_off(int b) const { return comb_off(kNBuf) + (size_t)b * 128; }
-    __host__ __device__ size_t part_off() const { return post_off(kNBuf); }                         // [2][kP2][8][36]
+    __host__ __device__ size_t comb_off(int b) const { return y_off(kNY) + (size_t)b * 512; }
+    __host__ __device__ size_t post_off(int b) const { return comb_off(kNY) + (size_t)b * 128; }
+    __host__ __device__ size_t part_off() const { return post_off(kNY); }                           // [2][kP2][8][36]
     __host__ __device__ size_t recv_off() const { return part_off() + (size_t)2 * kP2 * kG * kRec * 4; }  // [2][16][36]
     __host__ __device__ size_t prein_off() const { return recv_off() + (size_t)2 * kC * kRec * 4; }     // [kNPre][8][8]
     __host__ __device__ size_t gam_off() const { return prein_off() + (size_t)kNPre * kG * 8 * 4; }     // [Hs] bf16
     __host__ __device__ size_t bar_off() const { return gam_off() + (size_t)nHB * 64 * 2; }
-    // full[kNBuf], postd[kNBuf], part_full[2], pre_full[kNPre], parts_ready[2], parts_free[2]
-    static constexpr int kBars = 2 * kNBuf + 2 + kNPre + 4;
+    // full[kNBuf], postd[kNBuf], yfull[kNY], part_full[2], pre_full[kNPre], parts_ready[2], parts_free[2]
+    static constexpr int kBars = 2 * kNBuf + kNY + 2 + kNPre + 4;
     __host__ __device__ size_t tmem_off() const { return bar_off() + (size_t)kBars * 8; }
     __host__ __device__ size_t bytes() const { return tmem_off() + 8; }
 };
@@ -201,7 +202,8 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     float *sPreIn = reinterpret_cast<float *>(smem + L.prein_off());
     unsigned char *sGam = smem + L.gam_off();
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off());
-    uint64_t *full = bars, *postd = bars + kNBuf, *part_full = bars + 2 * kNBuf, *pre_full = bars + 2 * kNBuf + 2,
+    uint64_t *full = bars, *postd = bars + kNBuf, *yfull = postd + kNBuf, *part_full = yfull + kNY,
+             *pre_full = part_full + 2,
              *parts_ready = pre_full + kNPre, *parts_free = parts_ready + 2;
     uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.tmem_off());
 
@@ -224,6 +226,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     // ---- set-up
     if (warp == kWOwner) {
         if (lane == 0) {
+            for (int i = 0; i < kNY; ++i) mbar_init(&yfull[i], 1);
             for (int i = 0; i < kNBuf; ++i) {
                 mbar_init(&full[i], 1);
                 mbar_init(&postd[i], kP1);
@@ -306,8 +309,9 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 p_goff[k] = t * kHC * H + h0 + v * kVec;
             }
             for (int q = 0; q < n_it; ++q) {
-                const int b = q % kNBuf;
+                const int b = q % kNBuf, ys = q % kNY;
                 bwait(&full[b], (uint32_t)((q / kNBuf) & 1), dead);
+                bwait(&yfull[ys], (uint32_t)((q / kNY) & 1), dead);
                 unsigned char *rb = smem + L.r_off(b);
                 const int64_t t0 = group_t0(q);
                 uint16_t *rrow = R_out + t0 * kHC * (int64_t)H;
@@ -315,14 +319,14 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 for (int k = 0; k < kP1Items; ++k) {
                     const int t = p_t[k];
                     if (t < kG) {
-                        const float *cb = reinterpret_cast<const float *>(smem + L.comb_off(b)) + t * 16;
-                        const float *pb = reinterpret_cast<const float *>(smem + L.post_off(b)) + t * 4;
+                        const float *cb = reinterpret_cast<const float *>(smem + L.comb_off(ys)) + t * 16;
+                        const float *pb = reinterpret_cast<const float *>(smem + L.post_off(ys)) + t * 4;
                         unsigned char *rp = rb + p_roff[k];
                         uint4 r4[kHC], o[kHC];
                         float rf[kHC][8];
 #pragma unroll
                         for (int j = 0; j < kHC; ++j) r4[j] = *reinterpret_cast<const uint4 *>(rp + j * lay.s_j);
-                        const uint4 y = *reinterpret_cast<const uint4 *>(smem + L.y_off(b) + p_yoff[k]);
+                        const uint4 y = *reinterpret_cast<const uint4 *>(smem + L.y_off(ys) + p_yoff[k]);
                         post_vec8_x2(r4, y, cb, pb, o, rf);
 #pragma unroll
                         for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(rp + j * lay.s_j) = o[j];
@@ -447,12 +451,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         const int ct = tid - kWCB * 32, cw = warp - kWCB;
         constexpr int kStride = kCB * 32;
         uint64_t *rdy = kPost ? postd : full;
-        // Tensor copies of group q into ring slot q % kNBuf, shared by the four combine warps (one per
-        // SM sub-partition) so that no sub-partition's issue stalls behind all of them: warp cw copies
-        // R stream cw (one box, or the 64-wide blocks hb = cw mod 4 of the per-block layout), the Y
-        // blocks hb = cw mod 4, and warp 0 (1) the previous comb (post) mixes.  Warp 0 sets the
-        // expected byte count.
-        const uint32_t expect_bytes = (uint32_t)nHB * (4096 + (kPost ? 1024 : 0)) + (kPost ? 512 + 128 : 0);
+        // Tensor copies of group q's R tile into ring slot q % kNBuf, shared by the four combine warps
+        // (one per SM sub-partition): warp cw copies stream cw (one box) or the 64-wide blocks
+        // hb = cw mod 4 of the per-block layout.  Warp 0 sets the expected byte count.
+        const uint32_t expect_bytes = (uint32_t)nHB * 4096;
         auto issue = [&](int q) {
             const int b = q % kNBuf;
             const int t0 = (int)group_t0(q);
@@ -460,17 +462,9 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             unsigned char *rs = smem + L.r_off(b);
             if (lay.one_box) {
                 tma_load_4d(rs + cw * lay.s_j, &maps.R, 0, t0, h0 / 64, cw, &full[b]);
-                if (kPost)
-                    for (int hb = cw; hb < nHB; hb += kCB)
-                        tma_load_3d(smem + L.y_off(b) + hb * 1024, &maps.Y, 0, t0, h0 / 64 + hb, &full[b]);
             } else {
-                for (int hb = cw; hb < nHB; hb += kCB) {
-                    tma_load_3d(rs + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
-                    if (kPost) tma_load_2d(smem + L.y_off(b) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &full[b]);
-                }
+                for (int hb = cw; hb < nHB; hb += kCB) tma_load_3d(rs + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
             }
-            if (kPost && cw == 0) tma_load_2d(smem + L.comb_off(b), &maps.comb, 0, t0, &full[b]);
-            if (kPost && cw == 1) tma_load_2d(smem + L.post_off(b), &maps.post, 0, t0, &full[b]);
         };
         if (lane == 0)
             for (int q = 0; q < kNBuf && q < n_it; ++q) issue(q);
@@ -525,7 +519,24 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             dead = dead || drained;
         }
     } else if (warp == kWSend) {
-        // ================================ sender: records of the group from the projection partials
+        // ================================ sender: records of the group from the projection partials;
+        // also refills the Y ring: once group q's partials are in, the post is done with Y slot
+        // q % kNY, and lane 0 copies Y and the previous mixes of group q + kNY into it
+        const uint32_t ybytes = (uint32_t)nHB * 1024 + 512 + 128;
+        auto issue_y = [&](int q) {
+            const int ys = q % kNY;
+            const int t0 = (int)group_t0(q);
+            mbar_arrive_expect_tx(&yfull[ys], ybytes);
+            if (lay.one_box)
+                tma_load_3d(smem + L.y_off(ys), &maps.Y, 0, t0, h0 / 64, &yfull[ys]);
+            else
+                for (int hb = 0; hb < nHB; ++hb)
+                    tma_load_2d(smem + L.y_off(ys) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &yfull[ys]);
+            tma_load_2d(smem + L.comb_off(ys), &maps.comb, 0, t0, &yfull[ys]);
+            tma_load_2d(smem + L.post_off(ys), &maps.post, 0, t0, &yfull[ys]);
+        };
+        if (kPost && lane == 0)
+            for (int q = 0; q < kNY && q < n_it; ++q) issue_y(q);
         for (int q = 0; q < n_it; ++q) {
             bwait(&parts_ready[q & 1], (uint32_t)((q >> 1) & 1), dead);
             // chunk (token t, 16-byte piece qq) = lane + 32 k: sum of the warps' partials, fixed order
@@ -561,6 +572,17 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                                                        __float_as_uint(sum[k].z), __float_as_uint(sum[k].w)));
                 }
             }
+            if (kPost && lane == 0 && q + kNY < n_it && !dead) {
+                fence_proxy_async_smem();
+                issue_y(q + kNY);
+            }
+        }
+        if (kPost && lane == 0) {
+            // the last Y copies issued have landed (already true unless a wait timed out)
+            bool drained = false;
+            for (int q = n_it > kNY ? n_it - kNY : 0; q < n_it; ++q)
+                mbar_wait_timed(&yfull[q % kNY], (uint32_t)((q / kNY) & 1), drained, kWaitLimitNs);
+            dead = dead || drained;
         }
     } else {
         // ================================ owner
@@ -716,7 +738,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     const int nHB = Hs / 64;
     RLayout lay{1024, nHB * 1024, true};
     // R [T][4][H] bf16 as (h % 64, t, h / 64, j), one box {64, 8, nHB, 1} per stream and group, and
-    // Y [T][H] as (h % 64, t, h / 64), one box {64, 8, 1} per 64-wide block: needs H % 64 == 0
+    // Y [T][H] as (h % 64, t, h / 64), one box {64, 8, nHB} per group: needs H % 64 == 0
     // (otherwise a block would run into the next row instead of the zero fill)
     if (a.H % 64 != 0) lay.one_box = false;
     if (lay.one_box) {
@@ -727,7 +749,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     }
     if (lay.one_box && post) {
         const cuuint64_t dims[3] = {64, T, H / 64}, strides[2] = {H * 2, 128};
-        const cuuint32_t box[3] = {64, (cuuint32_t)kG, 1};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kG, (cuuint32_t)nHB};
         lay.one_box = encode(fn, &maps.Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Y, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B) == cudaSuccess;
     }

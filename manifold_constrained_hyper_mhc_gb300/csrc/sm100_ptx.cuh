@@ -65,7 +65,7 @@ __device__ __forceinline__ void mbar_wait_timed(uint64_t *bar, uint32_t parity, 
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         for (int i = 0; i < 8; ++i)
-            if (mbar_try_wait_hint(bar, parity, 1000u)) return;
+            if (mbar_try_wait_hint(bar, parity, 100u)) return;
         if (globaltimer_ns() - t0 > limit_ns) {
             dead = true;
             return;
