@@ -292,21 +292,22 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     if (warp < kP1) {
         // ================================ post: items (token, vector) pt + k * 224 of the group
         if (kPost) {
-            constexpr int kStride = kP1 * 32;
-            // consecutive items are consecutive vectors of one token, so every 8-lane wavefront reads
-            // and writes the 8 chunks of one 128-byte row: conflict-free.  The items are the same in
-            // every group: their offsets are computed once.
+            // token-major items: thread tid works on token tid / kTPT, vectors tid % kTPT + kTPT * k, so
+            // the token's mixes are loaded once per group; 8 consecutive lanes read and write 8
+            // consecutive chunks of a 128-byte row.  The items are the same in every group: their offsets
+            // are computed once.
+            constexpr int kTPT = kP1 * 32 / kG;  // threads per token (28)
+            const int p_tok = tid / kTPT;
             uint32_t p_roff[kP1Items], p_yoff[kP1Items];
-            int p_t[kP1Items], p_goff[kP1Items];
+            int p_goff[kP1Items];
+            bool p_on[kP1Items];
 #pragma unroll
             for (int k = 0; k < kP1Items; ++k) {
-                const int item = tid + k * kStride;
-                const int t = item / nvec, v = item % nvec;
-                const bool on = item < kG * nvec && h0 + v * kVec < H;
-                p_t[k] = on ? t : kG;  // kG: no item
-                p_roff[k] = r_swz(v >> 3, t, 0, v & 7, lay);
-                p_yoff[k] = y_swz(v >> 3, t, v & 7);
-                p_goff[k] = t * kHC * H + h0 + v * kVec;
+                const int v = tid % kTPT + kTPT * k;
+                p_on[k] = v < nvec && h0 + v * kVec < H;
+                p_roff[k] = r_swz(v >> 3, p_tok, 0, v & 7, lay);
+                p_yoff[k] = y_swz(v >> 3, p_tok, v & 7);
+                p_goff[k] = p_tok * kHC * H + h0 + v * kVec;
             }
             for (int q = 0; q < n_it; ++q) {
                 const int b = q % kNBuf, ys = q % kNY;
@@ -315,12 +316,23 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 unsigned char *rb = smem + L.r_off(b);
                 const int64_t t0 = group_t0(q);
                 uint16_t *rrow = R_out + t0 * kHC * (int64_t)H;
+                float cm[kHC * kHC], pm[kHC];
+                {
+                    const float4 *cb = reinterpret_cast<const float4 *>(smem + L.comb_off(ys)) + p_tok * 4;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const float4 f = cb[x];
+                        cm[4 * x] = f.x; cm[4 * x + 1] = f.y; cm[4 * x + 2] = f.z; cm[4 * x + 3] = f.w;
+                    }
+                    const float4 f = *(reinterpret_cast<const float4 *>(smem + L.post_off(ys)) + p_tok);
+                    pm[0] = f.x; pm[1] = f.y; pm[2] = f.z; pm[3] = f.w;
+                }
+                const int t = p_tok;
 #pragma unroll
                 for (int k = 0; k < kP1Items; ++k) {
-                    const int t = p_t[k];
-                    if (t < kG) {
-                        const float *cb = reinterpret_cast<const float *>(smem + L.comb_off(ys)) + t * 16;
-                        const float *pb = reinterpret_cast<const float *>(smem + L.post_off(ys)) + t * 4;
+                    if (p_on[k]) {
+                        const float *cb = cm;
+                        const float *pb = pm;
                         unsigned char *rp = rb + p_roff[k];
                         uint4 r4[kHC], o[kHC];
                         float rf[kHC][8];
@@ -468,19 +480,20 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         };
         if (lane == 0)
             for (int q = 0; q < kNBuf && q < n_it; ++q) issue(q);
-        // this thread's items (token, vector) item = ct + k * 128, the same in every group: shared
-        // memory offset of stream 0, token, X offset within the group's rows, RMSNorm weight offset
+        // token-major items: thread ct works on token ct / kCPT, vectors ct % kCPT + kCPT * k, so the
+        // token's (pre, rstd) is read once per group; offsets computed once
+        constexpr int kCPT = kStride / kG;  // threads per token (16)
+        const int c_tok = ct / kCPT;
         uint32_t c_roff[kCItems];
-        int c_t[kCItems], c_xoff[kCItems], c_v[kCItems];
+        int c_xoff[kCItems], c_v[kCItems];
+        bool c_on[kCItems];
 #pragma unroll
         for (int k = 0; k < kCItems; ++k) {
-            const int item = ct + k * kStride;
-            const int t = item / nvec, v = item % nvec;
-            const bool on = item < kG * nvec && h0 + v * kVec < H;
-            c_t[k] = on ? t : kG;  // kG: no item
+            const int v = ct % kCPT + kCPT * k;
+            c_on[k] = v < nvec && h0 + v * kVec < H;
             c_v[k] = v;
-            c_roff[k] = r_swz(v >> 3, t, 0, v & 7, lay);
-            c_xoff[k] = t * H + h0 + v * kVec;
+            c_roff[k] = r_swz(v >> 3, c_tok, 0, v & 7, lay);
+            c_xoff[k] = c_tok * H + h0 + v * kVec;
         }
         for (int q = 0; q < n_it; ++q) {
             const int b = q % kNBuf, s = q % kNPre;
@@ -491,13 +504,13 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             const unsigned char *rb = smem + L.r_off(b);
             const float *pin = sPreIn + (size_t)s * kG * 8;
             uint16_t *xrow = X_out + t0 * (int64_t)H;
+            const float4 pr = *reinterpret_cast<const float4 *>(pin + c_tok * 8);
+            const float rstd = pin[c_tok * 8 + 4];
+            const float pre[kHC] = {pr.x, pr.y, pr.z, pr.w};
+            const bool tok_ok = t0 + c_tok < T;
 #pragma unroll
             for (int k = 0; k < kCItems; ++k) {
-                const int t = c_t[k];
-                if (t < kG && t0 + t < T) {
-                    const float4 pr = *reinterpret_cast<const float4 *>(pin + t * 8);
-                    const float rstd = pin[t * 8 + 4];
-                    const float pre[kHC] = {pr.x, pr.y, pr.z, pr.w};
+                if (c_on[k] && tok_ok) {
                     const unsigned char *rp = rb + c_roff[k];
                     float rf[kHC][8], x[8];
 #pragma unroll

@@ -139,8 +139,14 @@ __device__ __forceinline__ void combine_vec8_x2(const float (&rf)[kHC][8], const
 __device__ __forceinline__ uint4 norm_vec8(const float (&x)[8], float rstd, uint4 g) {
     float G[8], o[8];
     unpack8(g, G);
+    // packed fp32 multiplies: each half is the same IEEE product as the scalar form
+    const float2 r2 = make_float2(rstd, rstd);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = (x[e] * rstd) * G[e];
+    for (int e = 0; e < 8; e += 2) {
+        const float2 v = __fmul2_rn(__fmul2_rn(make_float2(x[e], x[e + 1]), r2), make_float2(G[e], G[e + 1]));
+        o[e] = v.x;
+        o[e + 1] = v.y;
+    }
     return pack8_rn(o);
 }
 
