@@ -100,9 +100,12 @@ typedef enum mhc_schedule {
                                      in the steady state */
     MHC_SCHEDULE_PIPE2 = 7,       /* as PIPE, with the projection on tcgen05.mma (phi resident in
                                      tensor memory as the A operand) and the Sinkhorn batched at the end */
-    MHC_SCHEDULE_WS = 8           /* as PIPE with warp-specialised roles (TMA producer, post,
+    MHC_SCHEDULE_WS = 8,          /* as PIPE with warp-specialised roles (TMA producer, post,
                                      projection + Gram on the tensor cores, owner, combine) handing
-                                     groups over through mbarriers, and a 5-deep tile ring */
+                                     groups over through mbarriers, and a 6-deep tile ring */
+    MHC_SCHEDULE_SMALL = 9        /* T <= 64 only: one cooperative launch, one CTA per hidden slice
+                                     on up to every SM, one bounded grid barrier between the partial
+                                     sums and the combine (latency-bound decode calls) */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */
@@ -183,10 +186,12 @@ MHC_API mhc_status mhc_set_schedule(int schedule);
 /* The schedule AUTO would pick for (T, H) on the current device. */
 MHC_API int mhc_auto_schedule(int64_t T, int64_t H);
 
-/* Synchronises `stream`, then reads and clears the device status word kept in
- * the workspace: MHC_ERR_DEVICE_TIMEOUT if a bounded device-side wait gave up
- * since the last check (the workspace must then be zero-filled again),
- * MHC_ERR_CUDA if the stream reports an error, else MHC_OK. */
+/* Synchronises `stream`, then reads the device status word kept in the
+ * workspace: MHC_ERR_DEVICE_TIMEOUT if a bounded device-side wait gave up since
+ * the last check, MHC_ERR_CUDA if the stream reports an error, else MHC_OK.
+ * After a timeout it zero-fills the workspace's control block (the status word
+ * and the grid-barrier words a wait that gave up may leave mid-count), so the
+ * workspace is usable again. */
 MHC_API mhc_status mhc_check_status(void *workspace, void *stream);
 
 /* Number of kernels launched by the last call on this thread (0 if it failed

@@ -24,7 +24,7 @@ __all__ = [
 OK = 0
 STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
           -4: "MHC_ERR_CUDA", -5: "MHC_ERR_DEVICE_TIMEOUT"}
-SCHEDULES = {"auto": 0, "split": 1, "cluster": 2, "cluster_8x16": 3, "cluster_8x8": 4, "cluster16": 5, "pipe": 6, "pipe2": 7, "ws": 8}
+SCHEDULES = {"auto": 0, "split": 1, "cluster": 2, "cluster_8x16": 3, "cluster_8x8": 4, "cluster16": 5, "pipe": 6, "pipe2": 7, "ws": 8, "small": 9}
 
 
 class MhcError(RuntimeError):

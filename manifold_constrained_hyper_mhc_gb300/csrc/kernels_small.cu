@@ -1,0 +1,492 @@
+// Small-T schedule (schedule "small"): the whole mHC post+pre step in one
+// launch for decode-sized calls (T <= 64), built for latency rather than
+// bandwidth.
+//
+// The hidden dimension is split across up to one CTA per SM (slices of Hs
+// values, a multiple of 8; Hs = 64 at H = 7168, 112 CTAs).  CTA c:
+//   1. post: R' of its slice for all T tokens (same fp32 expression as every
+//      other schedule), kept in shared memory and written to HBM; its slice of
+//      phi (fp32, 4*Hs rows), of gamma and the previous mixes arrive by bulk
+//      copies issued first;
+//   2. per token, the 24 projection partials over the slice on the tensor
+//      cores (mma.sync bf16: R' is exact in bf16, phi is split into a bf16 high
+//      part and a bf16 remainder, fp32 accumulation), and the 10 Gram-matrix
+//      partials R'_i . R'_j in fp32, to workspace records;
+//   3. grid barrier (bounded in time; the launch is cooperative, so every CTA
+//      is resident);
+//   4. every CTA bulk-copies the pre-logit and Gram part of every record into
+//      shared memory and sums it over the CTAs in one fixed order, so all CTAs
+//      hold identical r, pre and rstd (sum_h X^2 = pre^T G pre);
+//   5. combine + RMSNorm of its slice from the R' in shared memory;
+//   meanwhile warp 0 of CTA c < T bulk-copies token c's records, sums them in
+//   the same order and finishes its mixes (pre, post, Sinkhorn residual mix),
+//   so the Sinkhorn runs beside phases 4 and 5 rather than after them.
+// phi is used in fp32 directly (no packing launch) and nothing is re-read from
+// HBM, so a call is a single launch.
+//
+// Workspace records, token-major so that one bulk copy fetches a token's (or a
+// token chunk's) records of every CTA:
+//   heads [T][nc][16]: pre logits 0..3, Gram entries (0,0) (1,1) (2,2) (3,3)
+//                      (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), two zeros;
+//   tails [T][nc][24]: logits 4..23, four zeros.
+#include <cstdint>
+
+#include "mhc_device.cuh"
+#include "mhc_kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace mhc {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kSNT = 256;  // threads per CTA
+constexpr int kHead = 16, kTail = 24;  // floats per record head / tail
+constexpr uint64_t kSpinLimitNs = 1000000000ull;
+constexpr int kBigBytes = 112 * 1024;  // shared memory for one token chunk of record heads
+constexpr size_t kSmallSmemLimit = 227 * 1024;
+
+// Tokens per chunk of the phase-4 reduction (the heads of nc records each), at
+// most 16 so that the chunk's (token, value, segment) items fit one buffer.
+__host__ __device__ inline int small_chunk(int T, int nc) {
+    int tc = kBigBytes / (nc * kHead * 4);
+    if (tc < 1) tc = 1;
+    if (tc > 16) tc = 16;
+    return tc < T ? tc : T;
+}
+
+struct SmallSmem {
+    int T, Hs, nc;
+    __host__ __device__ int tpad() const { return (T + 15) / 16 * 16; }
+    __host__ __device__ int rs() const { return kHC * Hs + 8; }  // R' row stride (elements), padded
+    __host__ __device__ size_t bar_off() const { return 0; }      // 4 mbarriers
+    __host__ __device__ size_t comb_off() const { return 64; }    // [T][16] fp32
+    __host__ __device__ size_t post_off() const { return comb_off() + (size_t)T * 64; }  // [T][4]
+    __host__ __device__ size_t rp_off() const { return post_off() + (size_t)T * 16; }    // [tpad][rs] bf16
+    __host__ __device__ size_t phi_off() const { return rp_off() + (size_t)tpad() * rs() * 2; }    // [4Hs][24] fp32
+    __host__ __device__ size_t gam_off() const { return phi_off() + (size_t)kHC * Hs * kNumMix * 4; }  // [Hs] bf16
+    __host__ __device__ size_t pp_off() const { return gam_off() + (size_t)Hs * 2; }         // [8 warps][16][24]
+    __host__ __device__ size_t gram_off() const { return pp_off() + 8 * 16 * kNumMix * 4; }  // [T][10]
+    __host__ __device__ size_t big_off() const {  // [tc][nc][16]
+        return gram_off() + (((size_t)T * 10 * 4 + 15) & ~size_t(15));
+    }
+    __host__ __device__ size_t ownh_off() const { return big_off() + (size_t)small_chunk(T, nc) * nc * kHead * 4; }
+    __host__ __device__ size_t ownt_off() const { return ownh_off() + (size_t)nc * kHead * 4; }  // [nc][24]
+    __host__ __device__ size_t sums_off() const { return ownt_off() + (size_t)nc * kTail * 4; }  // [T][16]
+    __host__ __device__ size_t st_off() const { return sums_off() + (size_t)T * 16 * 4; }        // [T][8]
+    __host__ __device__ size_t red_off() const { return st_off() + (size_t)T * 8 * 4; }          // [16][16][4]
+    __host__ __device__ size_t flag_off() const { return red_off() + 1024 * 4; }
+    __host__ __device__ size_t bytes() const { return flag_off() + 16; }
+};
+
+__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two fp32 values -> bf16 high parts (low half = first) and bf16 remainders.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack2_rn(x0, x1);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+    lo = pack2_rn(x0 - h0, x1 - h1);
+}
+
+// Grid barrier on a monotonic 64-bit arrival counter (zero before the first use;
+// every completed barrier leaves it at a multiple of the CTA count).  Release on
+// arrival, acquire on the poll.  Bounded in time: on a timeout it returns false.
+__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long n) {
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        unsigned long long old, cur;
+        asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
+        const unsigned long long target = (old / n + 1) * n;
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(ctr) : "memory");
+            if (cur >= target) break;
+            if (globaltimer_ns() - t0 > kSpinLimitNs) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    return ok;
+}
+
+// Sum over the CTAs in the one fixed order every sum of this schedule takes: four
+// segments of L4 consecutive CTAs, each summed in CTA order, then ((s0 + s1) + s2) + s3.
+// src[q * stride] is CTA q's value.
+__device__ __forceinline__ float cta_sum(const float *src, int stride, int nc, int L4) {
+    float seg[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int q0 = g * L4, q1 = q0 + L4 < nc ? q0 + L4 : nc;
+        float a = 0.f;
+#pragma unroll 8
+        for (int q = q0; q < q1; ++q) a += src[q * stride];
+        seg[g] = a;
+    }
+    return ((seg[0] + seg[1]) + seg[2]) + seg[3];
+}
+
+template <bool kPost>
+__global__ void __launch_bounds__(kSNT, 1)
+small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, const float *__restrict__ prev_post,
+             const float *__restrict__ prev_comb, const float *__restrict__ phi, const float *__restrict__ bias,
+             const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int T, int H,
+             int Hs, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
+             float *__restrict__ post_out, float *__restrict__ res_out, float *__restrict__ part,
+             unsigned int *__restrict__ ctrl) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, nc = gridDim.x;
+    const SmallSmem L{T, Hs, nc};
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar_off());  // 0 mixes+gamma, 1 phi, 2 heads, 3 owner
+    float *sComb = reinterpret_cast<float *>(sm + L.comb_off());
+    float *sPost = reinterpret_cast<float *>(sm + L.post_off());
+    uint16_t *sRp = reinterpret_cast<uint16_t *>(sm + L.rp_off());
+    float *sPhi = reinterpret_cast<float *>(sm + L.phi_off());
+    uint16_t *sGam = reinterpret_cast<uint16_t *>(sm + L.gam_off());
+    float *sPP = reinterpret_cast<float *>(sm + L.pp_off());
+    float *sGram = reinterpret_cast<float *>(sm + L.gram_off());
+    float *sBig = reinterpret_cast<float *>(sm + L.big_off());
+    float *sOwnH = reinterpret_cast<float *>(sm + L.ownh_off());
+    float *sOwnT = reinterpret_cast<float *>(sm + L.ownt_off());
+    float *sSums = reinterpret_cast<float *>(sm + L.sums_off());
+    float *sSt = reinterpret_cast<float *>(sm + L.st_off());
+    float *sRed = reinterpret_cast<float *>(sm + L.red_off());
+    int *sFlag = reinterpret_cast<int *>(sm + L.flag_off());
+    const int RS = L.rs();
+    const int h0 = c * Hs;
+    const int nvec = Hs / kVec;
+    const int hv = H - h0 < Hs ? H - h0 : Hs;  // valid hidden values of the slice (> 0, a multiple of 8)
+    float *heads = part;                           // [T][nc][16]
+    float *tails = part + (size_t)T * nc * kHead;  // [T][nc][24]
+    bool dead = false;
+
+    // ---- bulk copies: mixes + gamma (barrier 0), phi slice rows j*H + h0 .. (barrier 1)
+    if (tid == 0) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], (kPost ? T * 80u : 0u) + hv * 2u);
+        if (kPost) {
+            bulk_g2s(sComb, prev_comb, T * 64u, &bars[0]);
+            bulk_g2s(sPost, prev_post, T * 16u, &bars[0]);
+        }
+        bulk_g2s(sGam, gamma + h0, hv * 2u, &bars[0]);
+        mbar_arrive_expect_tx(&bars[1], kHC * hv * 96u);
+#pragma unroll
+        for (int j = 0; j < kHC; ++j)
+            bulk_g2s(sPhi + (size_t)j * Hs * kNumMix, phi + ((size_t)j * H + h0) * kNumMix, hv * 96u, &bars[1]);
+    }
+    if (hv < Hs)  // rows of the last slice beyond H: zero
+        for (int i = tid; i < kHC * (Hs - hv) * 6; i += kSNT) {
+            const int j = i / ((Hs - hv) * 6), r = i % ((Hs - hv) * 6);
+            *reinterpret_cast<float4 *>(sPhi + ((size_t)j * Hs + hv) * kNumMix + 4 * r) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+
+    // ---- 1. R' of the slice (zero beyond H), to shared memory and HBM.  The first item's rows
+    // are loaded before waiting for the mixes.
+    {
+        uint4 r4[kHC], y4 = make_uint4(0u, 0u, 0u, 0u);
+        const bool first_valid = tid < T * nvec && (tid % nvec) * kVec < hv;
+        if (first_valid) {
+            const int t = tid / nvec, v = tid % nvec;
+            const size_t base = (size_t)t * kHC * H + h0 + v * kVec;
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) r4[j] = ld_stream(R + base + (size_t)j * H);
+            if (kPost) y4 = ld_stream(Y + (size_t)t * H + h0 + v * kVec);
+        }
+        __syncthreads();  // barrier initialisation visible to every thread
+        mbar_wait_timed(&bars[0], 0, dead, kSpinLimitNs);
+        for (int item = tid; item < T * nvec; item += kSNT) {
+            const int t = item / nvec, v = item % nvec;
+            const size_t base = (size_t)t * kHC * H + h0 + v * kVec;
+            uint4 o[kHC];
+            if (v * kVec < hv) {
+                if (item != tid) {
+#pragma unroll
+                    for (int j = 0; j < kHC; ++j) r4[j] = ld_stream(R + base + (size_t)j * H);
+                    if (kPost) y4 = ld_stream(Y + (size_t)t * H + h0 + v * kVec);
+                }
+                if (kPost) {
+                    float rf[kHC][8];
+                    post_vec8_x2(r4, y4, sComb + t * 16, sPost + t * 4, o, rf);
+#pragma unroll
+                    for (int i = 0; i < kHC; ++i) st_stream(R_out + base + (size_t)i * H, o[i]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kHC; ++j) o[j] = r4[j];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kHC; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < kHC; ++j)
+                *reinterpret_cast<uint4 *>(sRp + (size_t)t * RS + j * Hs + v * kVec) = o[j];
+        }
+        mbar_wait_timed(&bars[1], 0, dead, kSpinLimitNs);
+        __syncthreads();
+    }
+
+    // ---- 2a. projection partials on the tensor cores: warp w takes m-tile (16 tokens) w / KW and
+    // the K-steps (16 rows of the 4*Hs) of share w % KW; its 16 x 24 result goes to sPP[w].
+    const int n_mt = (T + 15) / 16, KW = 8 / n_mt;
+    {
+        const int mt = warp / KW, kw = warp % KW;
+        if (mt < n_mt) {
+            const int nks = Hs / 4;  // 4*Hs / 16
+            const int k0 = kw * nks / KW, k1 = (kw + 1) * nks / KW;
+            float acc[3][4];
+#pragma unroll
+            for (int n = 0; n < 3; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+            const uint16_t *arow = sRp + (size_t)(mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * RS + 8 * (lane >> 4);
+            const int kr = (lane & 3) * 2, nn = lane >> 2;
+#pragma unroll 2
+            for (int ks = k0; ks < k1; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(arow + ks * 16, a);
+                const float *pb = sPhi + (size_t)(ks * 16 + kr) * kNumMix + nn;
+                float b[3][4];
+#pragma unroll
+                for (int n = 0; n < 3; ++n) {
+                    b[n][0] = pb[8 * n];
+                    b[n][1] = pb[kNumMix + 8 * n];
+                    b[n][2] = pb[8 * kNumMix + 8 * n];
+                    b[n][3] = pb[9 * kNumMix + 8 * n];
+                }
+#pragma unroll
+                for (int n = 0; n < 3; ++n) {
+                    uint32_t h01, l01, h89, l89;
+                    split2(b[n][0], b[n][1], h01, l01);
+                    split2(b[n][2], b[n][3], h89, l89);
+                    mma16816(acc[n], a, h01, h89);
+                    mma16816(acc[n], a, l01, l89);
+                }
+            }
+            float *dst = sPP + (size_t)warp * 16 * kNumMix;
+#pragma unroll
+            for (int n = 0; n < 3; ++n) {
+                const int col = 8 * n + kr;
+                *reinterpret_cast<float2 *>(dst + nn * kNumMix + col) = make_float2(acc[n][0], acc[n][1]);
+                *reinterpret_cast<float2 *>(dst + (nn + 8) * kNumMix + col) = make_float2(acc[n][2], acc[n][3]);
+            }
+        }
+    }
+    // ---- 2b. Gram partials in fp32: items (t, entry e), spread over the warps
+    {
+        constexpr uint64_t kIa = 0x2110003210ull, kIb = 0x3323213210ull;  // entry e -> (ia, ib), nibble e
+        for (int p = lane * 8 + warp; p < T * 10; p += kSNT) {
+            const int t = p / 10, e = p % 10;
+            const int ia = (int)(kIa >> (4 * e)) & 15, ib = (int)(kIb >> (4 * e)) & 15;
+            const uint16_t *ri = sRp + (size_t)t * RS + ia * Hs, *rj = sRp + (size_t)t * RS + ib * Hs;
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll 2
+            for (int u = 0; u < nvec; ++u) {
+                float a[8], b[8];
+                unpack8(*reinterpret_cast<const uint4 *>(ri + 8 * u), a);
+                unpack8(*reinterpret_cast<const uint4 *>(rj + 8 * u), b);
+                acc0 = __ffma2_rn(make_float2(a[0], a[1]), make_float2(b[0], b[1]), acc0);
+                acc1 = __ffma2_rn(make_float2(a[2], a[3]), make_float2(b[2], b[3]), acc1);
+                acc0 = __ffma2_rn(make_float2(a[4], a[5]), make_float2(b[4], b[5]), acc0);
+                acc1 = __ffma2_rn(make_float2(a[6], a[7]), make_float2(b[6], b[7]), acc1);
+            }
+            sGram[p] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        }
+    }
+    __syncthreads();
+    // ---- 2c. this CTA's records: K-shares of the projection in order, Gram entries
+    for (int i = tid; i < T * 40; i += kSNT) {
+        const int t = i / 40, s = i % 40;
+        float a = 0.f;
+        int n = -1;  // logit held in this slot
+        if (s < 4) n = s;
+        else if (s >= 16 && s < 36) n = s - 12;
+        if (n >= 0) {
+            const int mt = t >> 4, row = t & 15;
+            for (int kw = 0; kw < KW; ++kw) a += sPP[((size_t)(mt * KW + kw) * 16 + row) * kNumMix + n];
+        } else if (s >= 4 && s < 14) {
+            a = sGram[t * 10 + s - 4];
+        }
+        if (s < kHead) heads[((size_t)t * nc + c) * kHead + s] = a;
+        else tails[((size_t)t * nc + c) * kTail + s - kHead] = a;
+    }
+
+    // ---- 3. every CTA's records are in
+    __syncthreads();
+    const bool ok = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 16), (unsigned long long)nc);
+    if (tid == 0) sFlag[0] = ok ? 1 : 0;
+    __syncthreads();
+    if (!sFlag[0]) {
+        if (tid == 0) atomicOr(ctrl, 1u);
+        return;
+    }
+
+    const int L4 = (nc + 3) / 4;
+    const bool owner_cta = c < T;
+    if (owner_cta && warp == 0) {
+        // ---- token c (and c + nc, ...): pre logits, Gram diagonal and logits 4..23 summed over
+        // the CTAs; heads and the Sinkhorn mix.
+        int it = 0;
+        for (int t = c; t < T; t += nc, ++it) {
+            if (lane == 0) {
+                fence_proxy_async_global();
+                if (it > 0) fence_proxy_async_smem();  // the previous token's reads of the buffers are done
+                mbar_arrive_expect_tx(&bars[3], nc * (kHead + kTail) * 4u);
+                bulk_g2s(sOwnH, heads + (size_t)t * nc * kHead, nc * kHead * 4u, &bars[3]);
+                bulk_g2s(sOwnT, tails + (size_t)t * nc * kTail, nc * kTail * 4u, &bars[3]);
+            }
+            mbar_wait_timed(&bars[3], it & 1, dead, kSpinLimitNs);
+            // lane v < 28: value v = head slot v (v < 8) or logit v - 4 (tail slot v - 8)
+            float s = 0.f;
+            if (lane < 8) s = cta_sum(sOwnH + lane, kHead, nc, L4);
+            else if (lane < 28) s = cta_sum(sOwnT + (lane - 8), kTail, nc, L4);
+            float G[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) G[i] = __shfl_sync(0xffffffffu, s, 4 + i);
+            const float r = hc_rsqrt((G[0] + G[1]) + (G[2] + G[3]), H, sc.hc_norm_eps);
+            const float hi = __shfl_down_sync(0xffffffffu, s, 4);  // lane n >= 4: logit n = value n + 4
+            const float v = heads_and_sinkhorn(r * (lane < 4 ? s : hi), bias, mix_scales, sc);
+            if (lane < 4) pre_out[(size_t)t * 4 + lane] = v;
+            else if (lane < 8) post_out[(size_t)t * 4 + lane - 4] = v;
+            else if (lane < kNumMix) res_out[(size_t)t * 16 + lane - 8] = v;
+            __syncwarp();
+        }
+        if (dead && lane == 0) atomicOr(ctrl, 1u);
+        return;
+    }
+
+    // ---- 4. workers (every warp but an owner CTA's warp 0): pre logits and Gram entries of every
+    // token summed over the CTAs, in token chunks whose record heads are bulk-copied into shared
+    // memory first.
+    const int wbase = owner_cta ? 32 : 0, nwork = kSNT - wbase, wt = tid - wbase;
+    auto wsync = [&]() { asm volatile("bar.sync 1, %0;" ::"r"(nwork) : "memory"); };
+    {
+        const int TC = small_chunk(T, nc);
+        int it = 0;
+        for (int tc0 = 0; tc0 < T; tc0 += TC, ++it) {
+            const int tcn = T - tc0 < TC ? T - tc0 : TC;
+            if (wt == 0) {
+                fence_proxy_async_global();
+                if (it > 0) fence_proxy_async_smem();  // the previous chunk's reads of sBig are done
+                mbar_arrive_expect_tx(&bars[2], tcn * nc * kHead * 4u);
+                bulk_g2s(sBig, heads + (size_t)tc0 * nc * kHead, tcn * nc * kHead * 4u, &bars[2]);
+            }
+            mbar_wait_timed(&bars[2], it & 1, dead, kSpinLimitNs);
+            // items (tt, j, segment g) -> sRed[(tt * 16 + j) * 4 + g]
+            for (int p = wt; p < tcn * 64; p += nwork) {
+                const int j = p & 15, g = (p >> 4) & 3, tt = p >> 6;
+                const int q0 = g * L4, q1 = q0 + L4 < nc ? q0 + L4 : nc;
+                const float *src = sBig + (size_t)tt * nc * kHead + j;
+                float a = 0.f;
+#pragma unroll 8
+                for (int q = q0; q < q1; ++q) a += src[q * kHead];
+                sRed[(tt * 16 + j) * 4 + g] = a;
+            }
+            wsync();
+            for (int i = wt; i < tcn * 16; i += nwork) {
+                const float4 r4 = *reinterpret_cast<const float4 *>(sRed + 4 * i);
+                sSums[tc0 * 16 + i] = ((r4.x + r4.y) + r4.z) + r4.w;
+            }
+            wsync();
+        }
+    }
+    // r, pre and rstd of every token, one thread per token (identical in every CTA)
+    for (int t = wt; t < T; t += nwork) {
+        const float *s = sSums + t * 16;
+        float G[10];
+#pragma unroll
+        for (int e = 0; e < 10; ++e) G[e] = s[4 + e];
+        const float r = hc_rsqrt((G[0] + G[1]) + (G[2] + G[3]), H, sc.hc_norm_eps);
+        const float a_pre = mix_scales[0];
+        float pre[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pre[i] = pre_value(r * s[i], a_pre, bias[i]);
+        float sx = pre[0] * pre[0] * G[0] + pre[1] * pre[1] * G[1] + pre[2] * pre[2] * G[2] + pre[3] * pre[3] * G[3];
+        sx += 2.f * (pre[0] * pre[1] * G[4] + pre[0] * pre[2] * G[5] + pre[0] * pre[3] * G[6] +
+                     pre[1] * pre[2] * G[7] + pre[1] * pre[3] * G[8] + pre[2] * pre[3] * G[9]);
+        const float rstd = 1.f / sqrtf(fmaxf(sx, 0.f) / (float)H + sc.rmsnorm_eps);
+        *reinterpret_cast<float4 *>(sSt + t * 8) = make_float4(pre[0], pre[1], pre[2], pre[3]);
+        sSt[t * 8 + 4] = rstd;
+    }
+    wsync();
+
+    // ---- 5. combine + RMSNorm of the slice
+    for (int item = wt; item < T * nvec; item += nwork) {
+        const int t = item / nvec, v = item % nvec;
+        if (v * kVec >= hv) continue;
+        const float4 p4 = *reinterpret_cast<const float4 *>(sSt + t * 8);
+        const float pre[kHC] = {p4.x, p4.y, p4.z, p4.w};
+        float rf[kHC][8], x[8];
+#pragma unroll
+        for (int j = 0; j < kHC; ++j)
+            unpack8(*reinterpret_cast<const uint4 *>(sRp + (size_t)t * RS + j * Hs + v * kVec), rf[j]);
+        combine_vec8_x2(rf, pre, x);
+        st_stream(X_out + (size_t)t * H + h0 + v * kVec,
+                  norm_vec8(x, sSt[t * 8 + 4], *reinterpret_cast<const uint4 *>(sGam + v * kVec)));
+    }
+    if (dead && wt == 0) atomicOr(ctrl, 1u);
+}
+
+}  // namespace
+
+int small_ctas(int H, int num_sms) {
+    const int n = (H + 63) / 64;
+    return n < num_sms ? n : num_sms;
+}
+int small_slice(int H, int num_sms) {
+    const int n = small_ctas(H, num_sms);
+    return ((H + n - 1) / n + 7) / 8 * 8;
+}
+bool small_supported(int64_t T, int H, int num_sms) {
+    if (T < 1 || T > kSmallMaxT || num_sms < 1) return false;
+    const int Hs = small_slice(H, num_sms);
+    const int n = (H + Hs - 1) / Hs;
+    return SmallSmem{(int)T, Hs, n}.bytes() <= kSmallSmemLimit;
+}
+size_t small_workspace_bytes(int64_t T, int H) {
+    if (T < 1 || T > kSmallMaxT) return 0;
+    return (size_t)((H + 63) / 64) * (size_t)T * (kHead + kTail) * sizeof(float);
+}
+
+cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream) {
+    if (!small_supported(a.T, a.H, num_sms)) return cudaErrorInvalidValue;
+    const int Hs = small_slice(a.H, num_sms);
+    const int n = (a.H + Hs - 1) / Hs;  // every CTA holds at least one vector of the slice
+    const bool post = a.R_out != nullptr;
+    auto kern = post ? small_kernel<true> : small_kernel<false>;
+    const size_t smem = SmallSmem{(int)a.T, Hs, n}.bytes();
+    cudaError_t e;
+    if (smem > 48 * 1024 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+                                cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barrier cannot deadlock
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3((unsigned)n);
+    cfg.blockDim = dim3(kSNT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.bias, a.mix_scales, a.gamma,
+                              a.s, (int)a.T, a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, a.part,
+                              ctrl);
+}
+
+}  // namespace mhc

@@ -127,21 +127,26 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
         sched = std::max(sched, ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe_stash_bytes(T));
         sched = std::max(sched, ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe2_stash_bytes(T));
         sched = std::max(sched, ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::ws_stash_bytes(T));
+        sched = std::max(sched, mhc::small_workspace_bytes(T, (int)H));
     }
     size_t b = mhc::kControlBytes + sched;
     return (b + 255) & ~size_t(255);
 }
 
-int auto_schedule(int64_t /*T*/, int64_t H) {
+// Up to this many tokens the one-barrier small-T schedule has the lower latency.
+constexpr int64_t kSmallAutoMaxT = 32;
+
+int auto_schedule(int64_t T, int64_t H, int sms) {
+    if (T <= kSmallAutoMaxT && mhc::small_supported(T, (int)H, sms)) return MHC_SCHEDULE_SMALL;
     if (mhc::ws_supported((int)H)) return MHC_SCHEDULE_WS;
     if (mhc::pipe_supported((int)H)) return MHC_SCHEDULE_PIPE;
     return cluster_fits(kGeomDefault, H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
 }
 
-int choose_schedule(int64_t T, int64_t H) {
+int choose_schedule(int64_t T, int64_t H, int sms) {
     const int forced = g_forced_schedule.load(std::memory_order_relaxed);
     if (forced != MHC_SCHEDULE_AUTO) return forced;
-    return auto_schedule(T, H);
+    return auto_schedule(T, H, sms);
 }
 
 // Common body of the fused call (post != nullptr) and the pre-only call.
@@ -202,7 +207,7 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
 
     // mix_scales stays a device pointer: the kernels read the three alphas.
     mhc::Scalars s{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
-    const int sched = choose_schedule(T, H);
+    const int sched = choose_schedule(T, H, dev.sms);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     switch (sched) {
@@ -291,6 +296,22 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.C = 16; a.G = 8;
             e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
             g_launches = 2;
+            break;
+        }
+        case MHC_SCHEDULE_SMALL: {
+            if (!mhc::small_supported(T, (int)H, dev.sms))
+                return fail(MHC_ERR_UNSUPPORTED, "T=%lld, H=%lld does not fit the small schedule (T <= %d)",
+                            (long long)T, (long long)H, mhc::kSmallMaxT);
+            mhc::SplitArgs a{};
+            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
+            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+            a.T = T; a.H = (int)H; a.s = s;
+            a.R_out = fused ? residual_out : nullptr;
+            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.res_out = comb_res_mix_out;
+            a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            e = mhc::launch_small(a, static_cast<unsigned int *>(workspace), dev.sms, cs);
+            g_launches = 1;
             break;
         }
         case MHC_SCHEDULE_CLUSTER16: {
@@ -388,13 +409,18 @@ mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const f
 mhc_status mhc_set_schedule(int schedule) {
     if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER16 &&
         schedule != MHC_SCHEDULE_PIPE && schedule != MHC_SCHEDULE_PIPE2 && schedule != MHC_SCHEDULE_WS &&
+        schedule != MHC_SCHEDULE_SMALL &&
         geom_of(schedule) == nullptr)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);
     return MHC_OK;
 }
 
-int mhc_auto_schedule(int64_t T, int64_t H) { return auto_schedule(T, H); }
+int mhc_auto_schedule(int64_t T, int64_t H) {
+    Device dev;
+    if (current_device(dev) != MHC_OK) return MHC_SCHEDULE_AUTO;
+    return auto_schedule(T, H, dev.sms);
+}
 
 mhc_status mhc_check_status(void *workspace, void *stream) {
     if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
@@ -405,9 +431,10 @@ mhc_status mhc_check_status(void *workspace, void *stream) {
     e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
     if (word != 0) {
-        const uint32_t zero = 0;
-        e = cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status clear)");
+        // a wait that gave up can leave barrier words mid-count: clear the whole control block
+        e = cudaMemsetAsync(workspace, 0, mhc::kControlBytes, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(control block)");
         return fail(MHC_ERR_DEVICE_TIMEOUT, "device status word 0x%08x", word);
     }
     return MHC_OK;

@@ -88,6 +88,15 @@ size_t ws_pack_bytes(int H);
 size_t ws_stash_bytes(int64_t T);
 cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
 
+// Small-T schedule (kernels_small.cu): one cooperative launch, one CTA per hidden slice,
+// one grid barrier on a 64-bit arrival counter at control-block bytes 64..71.
+constexpr int kSmallMaxT = 64;
+int small_ctas(int H, int num_sms);
+int small_slice(int H, int num_sms);
+bool small_supported(int64_t T, int H, int num_sms);
+size_t small_workspace_bytes(int64_t T, int H);  // upper bound over SM counts
+cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);

@@ -47,7 +47,12 @@ def gpu_fused(mhc, R, Y, pp, pc, wd, sc=SC, **kw):
     return {k: (host_bf16(v) if v.dtype == torch.bfloat16 else host(v)) for k, v in o.items()}
 
 
+SMALL_MAX_T = 64  # the small-T schedule takes T <= 64 and refuses larger calls
+
+
 def check_workload(mhc, w, schedule="auto"):
+    if schedule == "small" and w.T > SMALL_MAX_T:
+        pytest.skip("the small schedule takes T <= 64")
     (phi, bias, ms, gamma), wd = weights_dev(w)
     R, Y, pp, pc = synth.tokens(w)
     mhc.set_schedule(schedule)
@@ -60,7 +65,7 @@ def check_workload(mhc, w, schedule="auto"):
     assert not msgs, "\n".join(msgs)
 
 
-ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws"]
+ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"]
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_verify", "mid_batch"])
@@ -131,14 +136,16 @@ def test_long_prefill_sampled_parity_and_invariants(mhc):
 def test_fused_equals_post_then_pre_bitwise(mhc, schedule):
     mhc.set_schedule(schedule)
     try:
-        _fused_vs_composed(mhc)
+        _fused_vs_composed(mhc, SMALL_MAX_T if schedule == "small" else None)
     finally:
         mhc.set_schedule("auto")
 
 
-def _fused_vs_composed(mhc):
+def _fused_vs_composed(mhc, max_t=None):
     for name in ("tiny", "mid_batch"):
         w = synth.WORKLOADS[name]
+        if max_t is not None and w.T > max_t:
+            continue
         _, wd = weights_dev(w)
         R, Y, pp, pc = synth.tokens(w)
         Rd, Yd, ppd, pcd = dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc)
@@ -259,3 +266,55 @@ def test_zero_tokens(mhc):
                              torch.empty((0, 4), device="cuda"), torch.empty((0, 4, 4), device="cuda"),
                              *wd, **SC)
     assert o["layer_in"].shape == (0, H)
+
+
+@pytest.mark.parametrize("H", [7168, 1024])
+def test_small_schedule_largest_T(mhc, H):
+    """The small-T schedule at its largest token count, against the oracle."""
+    check_workload(mhc, synth.Workload(f"small_{SMALL_MAX_T}x{H}", SMALL_MAX_T, H, 40, token_scale=True), "small")
+
+
+def test_small_schedule_refuses_large_T(mhc):
+    w = synth.Workload("small_65", SMALL_MAX_T + 1, 1024, 41)
+    _, wd = weights_dev(w)
+    R, Y, pp, pc = synth.tokens(w)
+    outs = {"layer_in": torch.full((w.T, w.H), 7, dtype=torch.int16, device="cuda").view(torch.bfloat16)}
+    mhc.set_schedule("small")
+    try:
+        with pytest.raises(mhc.MhcError) as ei:
+            mhc.shifted_post_pre(dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC, out=outs)
+    finally:
+        mhc.set_schedule("auto")
+    assert ei.value.status == -2
+    torch.cuda.synchronize()
+    assert bool((outs["layer_in"].view(torch.int16) == 7).all())
+
+
+def test_small_schedule_barrier_timeout_is_reported(mhc):
+    """The grid barrier's wait is bounded: with its arrival counter preset so that
+    it can never complete, every CTA gives up after its time limit, the call
+    leaves the status word set, mhc_check_status reports MHC_ERR_DEVICE_TIMEOUT
+    and clears the control block, and the next call on the same workspace is
+    correct again."""
+    w = synth.WORKLOADS["decode_verify"]
+    (phi, bias, ms, gamma), wd = weights_dev(w)
+    R, Y, pp, pc = synth.tokens(w)
+    args = (dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd)
+    ws = mhc.new_workspace(w.T, w.H)
+    words = ws.view(torch.int32)
+    mhc.set_schedule("small")
+    try:
+        words[16] = 0x40000000  # arrival counter far from the CTA count: the barrier never opens
+        mhc.shifted_post_pre(*args, **SC, workspace=ws)
+        with pytest.raises(mhc.MhcError) as ei:
+            mhc.check_status(ws)
+        assert ei.value.status == -5
+        assert int(words[:64].abs().sum()) == 0
+        o = mhc.shifted_post_pre(*args, **SC, workspace=ws)
+        mhc.check_status(ws)
+    finally:
+        mhc.set_schedule("auto")
+    got = {k: (host_bf16(v) if v.dtype == torch.bfloat16 else host(v)) for k, v in o.items()}
+    ref = oracle.shifted_post_pre(R, Y, pp, pc, phi, bias, ms, gamma, **SC, debug=True)
+    msgs = compare_fused(got, ref, (R, Y, pp, pc), gamma, label="after timeout")
+    assert not msgs, "\n".join(msgs)
