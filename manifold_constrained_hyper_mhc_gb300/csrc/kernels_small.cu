@@ -18,9 +18,9 @@
 //      shared memory and sums it over the CTAs in one fixed order, so all CTAs
 //      hold identical r, pre and rstd (sum_h X^2 = pre^T G pre);
 //   5. combine + RMSNorm of its slice from the R' in shared memory;
-//   meanwhile warp 0 of CTA c < T bulk-copies token c's records, sums them in
-//   the same order and finishes its mixes (pre, post, Sinkhorn residual mix),
-//   so the Sinkhorn runs beside phases 4 and 5 rather than after them.
+//   meanwhile warp 0 of CTA c < T bulk-copies token c's other 20 logits, sums
+//   them, takes r and the pre logits from phase 4 and finishes its mixes (pre,
+//   post, Sinkhorn residual mix), so the Sinkhorn runs beside phase 5.
 // phi is used in fp32 directly (no packing launch) and nothing is re-read from
 // HBM, so a call is a single launch.
 //
@@ -44,11 +44,11 @@ using namespace ptx;
 constexpr int kSNT = 256;  // threads per CTA
 constexpr int kHead = 16, kTail = 24;  // floats per record head / tail
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
-constexpr int kBigBytes = 112 * 1024;  // shared memory for one token chunk of record heads
+constexpr int kBigBytes = 100 * 1024;  // shared memory for one token chunk of record heads
 constexpr size_t kSmallSmemLimit = 227 * 1024;
+constexpr int kMaxCtas = 160;  // CTAs at most (one per SM)
 
-// Tokens per chunk of the phase-4 reduction (the heads of nc records each), at
-// most 16 so that the chunk's (token, value, segment) items fit one buffer.
+// Tokens per chunk of the phase-4 reduction (the heads of nc records each), at most 16.
 __host__ __device__ inline int small_chunk(int T, int nc) {
     int tc = kBigBytes / (nc * kHead * 4);
     if (tc < 1) tc = 1;
@@ -71,12 +71,13 @@ struct SmallSmem {
     __host__ __device__ size_t big_off() const {  // [tc][nc][16]
         return gram_off() + (((size_t)T * 10 * 4 + 15) & ~size_t(15));
     }
-    __host__ __device__ size_t ownh_off() const { return big_off() + (size_t)small_chunk(T, nc) * nc * kHead * 4; }
-    __host__ __device__ size_t ownt_off() const { return ownh_off() + (size_t)nc * kHead * 4; }  // [nc][24]
+    __host__ __device__ size_t ownt_off() const {  // [nc][24]
+        return big_off() + (size_t)small_chunk(T, nc) * nc * kHead * 4;
+    }
     __host__ __device__ size_t sums_off() const { return ownt_off() + (size_t)nc * kTail * 4; }  // [T][16]
     __host__ __device__ size_t st_off() const { return sums_off() + (size_t)T * 16 * 4; }        // [T][8]
-    __host__ __device__ size_t red_off() const { return st_off() + (size_t)T * 8 * 4; }          // [16][16][4]
-    __host__ __device__ size_t flag_off() const { return red_off() + 1024 * 4; }
+    __host__ __device__ size_t tl_off() const { return st_off() + (size_t)T * 8 * 4; }           // [32]
+    __host__ __device__ size_t flag_off() const { return tl_off() + 32 * 4; }
     __host__ __device__ size_t bytes() const { return flag_off() + 16; }
 };
 
@@ -92,6 +93,9 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 // Two fp32 values -> bf16 high parts (low half = first) and bf16 remainders.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
@@ -122,20 +126,39 @@ __device__ bool grid_barrier(unsigned long long *ctr, unsigned long long n) {
     return ok;
 }
 
-// Sum over the CTAs in the one fixed order every sum of this schedule takes: four
-// segments of L4 consecutive CTAs, each summed in CTA order, then ((s0 + s1) + s2) + s3.
-// src[q * stride] is CTA q's value.
-__device__ __forceinline__ float cta_sum(const float *src, int stride, int nc, int L4) {
-    float seg[4];
+// Warp-wide sum over the CTAs of 16 adjacent values, src[q * stride + 0..15] for CTA
+// q < nc (16-byte aligned rows).  Lane (quad j4 = lane & 3, group g = lane >> 2) adds
+// CTAs q = g, g + 8, g + 16, ... in that order from zero (its loads issued together,
+// slots past the last CTA adding zero); then an xor tree over the eight groups.  Every
+// lane returns the total of its quad, bit-identical across the lanes that share the quad
+// (each tree step adds the same two values) and across CTAs.  quads < 4 limits the
+// quads read.
+__device__ __forceinline__ float4 warp_cta_sum16(const float *src, int stride, int nc, int quads) {
+    const int lane = threadIdx.x & 31, j4 = lane & 3, g = lane >> 2;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kPer = kMaxCtas / 8, kHalf = kPer / 2;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const int q0 = g * L4, q1 = q0 + L4 < nc ? q0 + L4 : nc;
-        float a = 0.f;
-#pragma unroll 8
-        for (int q = q0; q < q1; ++q) a += src[q * stride];
-        seg[g] = a;
+    for (int h = 0; h < kPer; h += kHalf) {
+        float4 v[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) {
+            const int q = g + 8 * (h + i);
+            v[i] = q < nc && j4 < quads ? *reinterpret_cast<const float4 *>(src + (size_t)q * stride + 4 * j4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) a = add4(a, v[i]);
     }
-    return ((seg[0] + seg[1]) + seg[2]) + seg[3];
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+        float4 o;
+        o.x = __shfl_xor_sync(0xffffffffu, a.x, m);
+        o.y = __shfl_xor_sync(0xffffffffu, a.y, m);
+        o.z = __shfl_xor_sync(0xffffffffu, a.z, m);
+        o.w = __shfl_xor_sync(0xffffffffu, a.w, m);
+        a = add4(a, o);
+    }
+    return a;
 }
 
 template <bool kPost>
@@ -159,11 +182,10 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
     float *sPP = reinterpret_cast<float *>(sm + L.pp_off());
     float *sGram = reinterpret_cast<float *>(sm + L.gram_off());
     float *sBig = reinterpret_cast<float *>(sm + L.big_off());
-    float *sOwnH = reinterpret_cast<float *>(sm + L.ownh_off());
     float *sOwnT = reinterpret_cast<float *>(sm + L.ownt_off());
     float *sSums = reinterpret_cast<float *>(sm + L.sums_off());
     float *sSt = reinterpret_cast<float *>(sm + L.st_off());
-    float *sRed = reinterpret_cast<float *>(sm + L.red_off());
+    float *sTl = reinterpret_cast<float *>(sm + L.tl_off());
     int *sFlag = reinterpret_cast<int *>(sm + L.flag_off());
     const int RS = L.rs();
     const int h0 = c * Hs;
@@ -294,18 +316,28 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
             const int t = p / 10, e = p % 10;
             const int ia = (int)(kIa >> (4 * e)) & 15, ib = (int)(kIb >> (4 * e)) & 15;
             const uint16_t *ri = sRp + (size_t)t * RS + ia * Hs, *rj = sRp + (size_t)t * RS + ib * Hs;
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll 2
-            for (int u = 0; u < nvec; ++u) {
-                float a[8], b[8];
-                unpack8(*reinterpret_cast<const uint4 *>(ri + 8 * u), a);
-                unpack8(*reinterpret_cast<const uint4 *>(rj + 8 * u), b);
-                acc0 = __ffma2_rn(make_float2(a[0], a[1]), make_float2(b[0], b[1]), acc0);
-                acc1 = __ffma2_rn(make_float2(a[2], a[3]), make_float2(b[2], b[3]), acc1);
-                acc0 = __ffma2_rn(make_float2(a[4], a[5]), make_float2(b[4], b[5]), acc0);
-                acc1 = __ffma2_rn(make_float2(a[6], a[7]), make_float2(b[6], b[7]), acc1);
+            float2 acc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+            for (int u0 = 0; u0 < nvec; u0 += 4) {  // four vectors' loads issued together
+                uint4 va[4], vb[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const bool in = u0 + k < nvec;
+                    va[k] = in ? *reinterpret_cast<const uint4 *>(ri + 8 * (u0 + k)) : make_uint4(0u, 0u, 0u, 0u);
+                    vb[k] = in ? *reinterpret_cast<const uint4 *>(rj + 8 * (u0 + k)) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float a[8], b[8];
+                    unpack8(va[k], a);
+                    unpack8(vb[k], b);
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        acc[k] = __ffma2_rn(make_float2(a[e], a[e + 1]), make_float2(b[e], b[e + 1]), acc[k]);
+                }
             }
-            sGram[p] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            sGram[p] = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         }
     }
     __syncthreads();
@@ -316,9 +348,13 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         int n = -1;  // logit held in this slot
         if (s < 4) n = s;
         else if (s >= 16 && s < 36) n = s - 12;
-        if (n >= 0) {
+        if (n >= 0) {  // the K-shares in order (loads issued together; shares past KW add zero)
             const int mt = t >> 4, row = t & 15;
-            for (int kw = 0; kw < KW; ++kw) a += sPP[((size_t)(mt * KW + kw) * 16 + row) * kNumMix + n];
+            float v[8];
+#pragma unroll
+            for (int kw = 0; kw < 8; ++kw) v[kw] = kw < KW ? sPP[((size_t)(mt * KW + kw) * 16 + row) * kNumMix + n] : 0.f;
+#pragma unroll
+            for (int kw = 0; kw < 8; ++kw) a += v[kw];
         } else if (s >= 4 && s < 14) {
             a = sGram[t * 10 + s - 4];
         }
@@ -336,31 +372,30 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         return;
     }
 
-    const int L4 = (nc + 3) / 4;
     const bool owner_cta = c < T;
     if (owner_cta && warp == 0) {
-        // ---- token c (and c + nc, ...): pre logits, Gram diagonal and logits 4..23 summed over
-        // the CTAs; heads and the Sinkhorn mix.
+        // ---- token c (and c + nc, ...): logits 4..23 summed over the CTAs; pre logits and r from
+        // the workers' sums; heads and the Sinkhorn mix.
         int it = 0;
         for (int t = c; t < T; t += nc, ++it) {
             if (lane == 0) {
                 fence_proxy_async_global();
-                if (it > 0) fence_proxy_async_smem();  // the previous token's reads of the buffers are done
-                mbar_arrive_expect_tx(&bars[3], nc * (kHead + kTail) * 4u);
-                bulk_g2s(sOwnH, heads + (size_t)t * nc * kHead, nc * kHead * 4u, &bars[3]);
+                if (it > 0) fence_proxy_async_smem();  // the previous token's reads of the buffer are done
+                mbar_arrive_expect_tx(&bars[3], nc * kTail * 4u);
                 bulk_g2s(sOwnT, tails + (size_t)t * nc * kTail, nc * kTail * 4u, &bars[3]);
             }
             mbar_wait_timed(&bars[3], it & 1, dead, kSpinLimitNs);
-            // lane v < 28: value v = head slot v (v < 8) or logit v - 4 (tail slot v - 8)
-            float s = 0.f;
-            if (lane < 8) s = cta_sum(sOwnH + lane, kHead, nc, L4);
-            else if (lane < 28) s = cta_sum(sOwnT + (lane - 8), kTail, nc, L4);
-            float G[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) G[i] = __shfl_sync(0xffffffffu, s, 4 + i);
-            const float r = hc_rsqrt((G[0] + G[1]) + (G[2] + G[3]), H, sc.hc_norm_eps);
-            const float hi = __shfl_down_sync(0xffffffffu, s, 4);  // lane n >= 4: logit n = value n + 4
-            const float v = heads_and_sinkhorn(r * (lane < 4 ? s : hi), bias, mix_scales, sc);
+            {
+                const float4 a = warp_cta_sum16(sOwnT, kTail, nc, 4);       // logits 4..19
+                const float4 b = warp_cta_sum16(sOwnT + 16, kTail, nc, 1);  // logits 20..23
+                if (lane < 4) *reinterpret_cast<float4 *>(sTl + 4 * lane) = a;
+                if (lane == 0) *reinterpret_cast<float4 *>(sTl + 16) = b;
+            }
+            __syncwarp();
+            const float tl = lane >= 4 && lane < kNumMix ? sTl[lane - 4] : 0.f;  // lane n: logit n
+            if (it == 0) asm volatile("bar.sync 2, %0;" ::"r"(kSNT) : "memory");  // workers' sums are in
+            const float z = sSt[t * 8 + 5] * (lane < 4 ? sSums[t * 16 + lane] : tl);
+            const float v = heads_and_sinkhorn(z, bias, mix_scales, sc);
             if (lane < 4) pre_out[(size_t)t * 4 + lane] = v;
             else if (lane < 8) post_out[(size_t)t * 4 + lane - 4] = v;
             else if (lane < kNumMix) res_out[(size_t)t * 16 + lane - 8] = v;
@@ -387,20 +422,10 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
                 bulk_g2s(sBig, heads + (size_t)tc0 * nc * kHead, tcn * nc * kHead * 4u, &bars[2]);
             }
             mbar_wait_timed(&bars[2], it & 1, dead, kSpinLimitNs);
-            // items (tt, j, segment g) -> sRed[(tt * 16 + j) * 4 + g]
-            for (int p = wt; p < tcn * 64; p += nwork) {
-                const int j = p & 15, g = (p >> 4) & 3, tt = p >> 6;
-                const int q0 = g * L4, q1 = q0 + L4 < nc ? q0 + L4 : nc;
-                const float *src = sBig + (size_t)tt * nc * kHead + j;
-                float a = 0.f;
-#pragma unroll 8
-                for (int q = q0; q < q1; ++q) a += src[q * kHead];
-                sRed[(tt * 16 + j) * 4 + g] = a;
-            }
-            wsync();
-            for (int i = wt; i < tcn * 16; i += nwork) {
-                const float4 r4 = *reinterpret_cast<const float4 *>(sRed + 4 * i);
-                sSums[tc0 * 16 + i] = ((r4.x + r4.y) + r4.z) + r4.w;
+            // one warp per token of the chunk
+            for (int tt = wt >> 5; tt < tcn; tt += nwork >> 5) {
+                const float4 a = warp_cta_sum16(sBig + (size_t)tt * nc * kHead, kHead, nc, 4);
+                if (lane < 4) *reinterpret_cast<float4 *>(sSums + (tc0 + tt) * 16 + 4 * lane) = a;
             }
             wsync();
         }
@@ -422,8 +447,10 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         const float rstd = 1.f / sqrtf(fmaxf(sx, 0.f) / (float)H + sc.rmsnorm_eps);
         *reinterpret_cast<float4 *>(sSt + t * 8) = make_float4(pre[0], pre[1], pre[2], pre[3]);
         sSt[t * 8 + 4] = rstd;
+        sSt[t * 8 + 5] = r;
     }
     wsync();
+    if (owner_cta) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums and stats -> owner warp
 
     // ---- 5. combine + RMSNorm of the slice
     for (int item = wt; item < T * nvec; item += nwork) {
@@ -456,6 +483,7 @@ bool small_supported(int64_t T, int H, int num_sms) {
     if (T < 1 || T > kSmallMaxT || num_sms < 1) return false;
     const int Hs = small_slice(H, num_sms);
     const int n = (H + Hs - 1) / Hs;
+    if (n > kMaxCtas) return false;
     return SmallSmem{(int)T, Hs, n}.bytes() <= kSmallSmemLimit;
 }
 size_t small_workspace_bytes(int64_t T, int H) {

@@ -175,42 +175,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 // Sinkhorn normalisation of one positive 4x4 matrix held in registers
 // (row-major M[4a+c]): sinkhorn_iters times, each row then each column is
-// multiplied by the reciprocal of (sum + sinkhorn_eps).  The matrix is kept as
-// eight fp32 pairs P[2a] = (M[4a], M[4a+1]), P[2a+1] = (M[4a+2], M[4a+3]) and
-// worked on with packed fp32x2 adds and multiplies (each half the same IEEE
-// operation as the scalar one).  Sums are taken as: row a = ((M[4a] + M[4a+2]) +
-// (M[4a+1] + M[4a+3])) + eps; column c = ((M[c] + M[4+c]) + (M[8+c] + M[12+c]))
-// + eps.  The hardware reciprocal keeps the dependent chain short (the
-// correctly rounded one is a long instruction sequence); its error is within
-// 1 ulp per step.
+// multiplied by the reciprocal of (sum + sinkhorn_eps); sums are taken in the
+// order ((m0 + m1) + (m2 + m3)).  The hardware reciprocal keeps the dependent
+// chain short (the correctly rounded one is a long instruction sequence); its
+// error is within 1 ulp per step.
 __device__ __forceinline__ void sinkhorn16(float (&M)[16], const Scalars &s) {
-    float2 P[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) P[k] = make_float2(M[2 * k], M[2 * k + 1]);
-    const float2 e2 = make_float2(s.sinkhorn_eps, s.sinkhorn_eps);
     for (int it = 0; it < s.sinkhorn_iters; ++it) {
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const float2 v = __fadd2_rn(P[2 * a], P[2 * a + 1]);
-            const float inv = rcp_approx((v.x + v.y) + s.sinkhorn_eps);
-            const float2 i2 = make_float2(inv, inv);
-            P[2 * a] = __fmul2_rn(P[2 * a], i2);
-            P[2 * a + 1] = __fmul2_rn(P[2 * a + 1], i2);
-        }
-        const float2 c01 = __fadd2_rn(__fadd2_rn(__fadd2_rn(P[0], P[2]), __fadd2_rn(P[4], P[6])), e2);
-        const float2 c23 = __fadd2_rn(__fadd2_rn(__fadd2_rn(P[1], P[3]), __fadd2_rn(P[5], P[7])), e2);
-        const float2 i01 = make_float2(rcp_approx(c01.x), rcp_approx(c01.y));
-        const float2 i23 = make_float2(rcp_approx(c23.x), rcp_approx(c23.y));
+            const float inv = rcp_approx(((M[4 * a] + M[4 * a + 1]) + (M[4 * a + 2] + M[4 * a + 3])) + s.sinkhorn_eps);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            P[2 * a] = __fmul2_rn(P[2 * a], i01);
-            P[2 * a + 1] = __fmul2_rn(P[2 * a + 1], i23);
+            for (int c = 0; c < 4; ++c) M[4 * a + c] *= inv;
         }
-    }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        M[2 * k] = P[k].x;
-        M[2 * k + 1] = P[k].y;
+        for (int c = 0; c < 4; ++c) {
+            const float inv = rcp_approx(((M[c] + M[4 + c]) + (M[8 + c] + M[12 + c])) + s.sinkhorn_eps);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) M[4 * a + c] *= inv;
+        }
     }
 }
 
