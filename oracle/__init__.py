@@ -58,6 +58,16 @@ def _load():
             lib.oracle_shifted_post_pre.argtypes = [P, P, P, P, P, P, P, P, I64, I64,
                                                     D, D, D, D, I, P, P, P, P, P, P, P, P, I]
             lib.oracle_shifted_post_pre.restype = I
+            lib.oracle_e4m3_encode.argtypes = [D]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_decode.restype = D
+            lib.oracle_mx_scale_exp.argtypes = [D, I]
+            lib.oracle_mx_scale_exp.restype = I
+            lib.oracle_mx_scale_offset.argtypes = [I64, I64, I64]
+            lib.oracle_mx_scale_offset.restype = I64
+            lib.oracle_mxfp8_quantize.argtypes = [P, I64, I64, I, P, P]
+            lib.oracle_mxfp8_quantize.restype = I
             _lib = lib
     return _lib
 
@@ -155,3 +165,39 @@ def shifted_post_pre(R, Y, prev_post, prev_comb, phi, bias, mix_scales, gamma, *
     if debug:
         out.update(z=z, r=r, rstd=rstd)
     return out
+
+
+# ---- MXFP8 quantize of the layer input (see mhc_oracle.c for the readings) ----
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def e4m3_decode(b: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(b)))
+
+
+def mx_scale_exp(amax: float, mode: int) -> int:
+    return int(_load().oracle_mx_scale_exp(float(amax), int(mode)))
+
+
+def mx_scale_offset(m: int, k: int, H: int) -> int:
+    return int(_load().oracle_mx_scale_offset(int(m), int(k), int(H)))
+
+
+def mx_scale_shape(T: int, H: int):
+    """Padded (rows, block columns) of the 128 x 4 tile layout; bytes = rows * cols."""
+    return (T + 127) // 128 * 128, (H // 32 + 3) // 4 * 4
+
+
+def mxfp8_quantize(X, mode: int):
+    """X: [T, H] bf16 bits.  Returns (q [T, H] uint8 E4M3 codes, scales flat uint8 in the
+    tile layout, padding zero)."""
+    X = _c(X, np.uint16)
+    T, H = X.shape
+    rows, cols = mx_scale_shape(T, H)
+    q = np.zeros((T, H), np.uint8)
+    sc = np.zeros(rows * cols, np.uint8)
+    rc = _load().oracle_mxfp8_quantize(_p(X), T, H, int(mode), _p(q), _p(sc))
+    assert rc == 0
+    return q, sc

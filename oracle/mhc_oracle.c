@@ -302,3 +302,94 @@ int oracle_shifted_post_pre(const uint16_t *R, const uint16_t *Y, const float *p
     j.z = z; j.r = r; j.rstd = rstd;
     return run(j, T, nthreads);
 }
+
+/* ---- MXFP8 quantize of the layer input --------------------------------------------------
+ * [P3] "What changed" item 3: the mHC combine+RMSNorm output, written in bf16, was re-read by a
+ * separate MXFP8 quantize; the epilogue emits the quantized form directly.  "Correctness": the
+ * epilogue's bf16 output, FP8 values and swizzled UE8M0 scale block equal those of the bf16
+ * output followed by the separate quantize.  So the quantize consumes the bf16-rounded layer
+ * input, 32 consecutive hidden values of one token per block.
+ * The pages give no formula.  Readings (listed with the design notes):
+ *   - element format E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *     infinities; largest finite 448 = 1.75 * 2^8, smallest normal 2^-6, subnormals
+ *     k/8 * 2^-6), conversion by round to nearest even, finite values beyond 448 saturate;
+ *   - block scale 2^E stored as the byte E + 127 (UE8M0), with E from the block's largest
+ *     magnitude amax by one of two rules: mode 0 E = floor(log2 amax) - 8 (the largest
+ *     element lands in [256, 512) and may saturate); mode 1 the smallest E with
+ *     amax <= 448 * 2^E (never saturates).  amax == 0 gives E = -127; E is clamped to
+ *     [-127, 127];
+ *   - element = E4M3(x / 2^E), the division exact;
+ *   - scale bytes in the 128 x 4 tile layout: token m, block k at
+ *     ((m / 128) * KT + k / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + k % 4,
+ *     KT = ceil(H / 128); rows padded to a multiple of 128, blocks to a multiple of 4. */
+
+uint8_t oracle_e4m3_encode(double v)
+{
+    if (isnan(v)) return 0x7F;
+    uint8_t s = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a >= 448.0) return s | 0x7E;             /* largest finite, also the saturation value */
+    if (a == 0.0) return s;
+    int e;
+    frexp(a, &e);                                /* a in [2^(e-1), 2^e) */
+    int be = e - 1 < -6 ? -6 : e - 1;            /* binade exponent; subnormals share 2^-6's quantum */
+    double quantum = ldexp(1.0, be - 3);
+    double q = a / quantum;                      /* exact */
+    double r = floor(q), frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    double val = r * quantum;                    /* <= 448: a < 448 rounds to at most 448 */
+    if (val == 0.0) return s;
+    int ve;
+    frexp(val, &ve);
+    int vb = ve - 1;
+    if (vb < -6) return s | (uint8_t)(val / ldexp(1.0, -9));      /* subnormal: k * 2^-9 */
+    int mant = (int)((val / ldexp(1.0, vb) - 1.0) * 8.0);
+    return s | (uint8_t)(((vb + 7) << 3) | mant);
+}
+
+double oracle_e4m3_decode(uint8_t b)
+{
+    double sign = (b & 0x80) ? -1.0 : 1.0;
+    int ef = (b >> 3) & 0xF, m = b & 7;
+    if (ef == 0xF && m == 7) return NAN;
+    if (ef == 0) return sign * ldexp((double)m, -9);
+    return sign * ldexp(1.0 + m / 8.0, ef - 7);
+}
+
+int oracle_mx_scale_exp(double amax, int mode)
+{
+    if (!(amax > 0.0)) return -127;
+    int e;
+    double m = frexp(amax, &e);                  /* amax = (2m) * 2^(e-1), 2m in [1, 2) */
+    int fl = e - 1;
+    int E = (mode == 0) ? fl - 8 : (2.0 * m <= 1.75 ? fl - 8 : fl - 7);
+    if (E < -127) E = -127;
+    if (E > 127) E = 127;
+    return E;
+}
+
+int64_t oracle_mx_scale_offset(int64_t m, int64_t k, int64_t H)
+{
+    int64_t kt = (H / 32 + 3) / 4;
+    return ((m / 128) * kt + k / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + k % 4;
+}
+
+int oracle_mxfp8_quantize(const uint16_t *X /* [T][H] bf16 */, int64_t T, int64_t H, int mode,
+                          uint8_t *q /* [T][H] */, uint8_t *scales /* tile layout */)
+{
+    if (H % 32 != 0 || (mode != 0 && mode != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t k = 0; k < H / 32; ++k) {
+            const uint16_t *x = X + t * H + k * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(oracle_bf16_to_double(x[i]));
+                if (a > amax) amax = a;
+            }
+            int E = oracle_mx_scale_exp(amax, mode);
+            scales[oracle_mx_scale_offset(t, k, H)] = (uint8_t)(E + 127);
+            for (int i = 0; i < 32; ++i)
+                q[t * H + k * 32 + i] = oracle_e4m3_encode(ldexp(oracle_bf16_to_double(x[i]), -E));
+        }
+    return 0;
+}

@@ -417,3 +417,108 @@ def test_synthetic_inputs_are_reproducible_by_block():
     np.testing.assert_allclose(pc.sum(1), 1, atol=1e-6)
     np.testing.assert_allclose(pc.sum(2), 1, atol=1e-6)
     assert np.all(pc > 0) and np.all((pp > 0) & (pp < 2))
+
+
+# ---------------------------------------------------------------- MXFP8 quantize
+# E4M3 facts from the format definition (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+# no infinities, S.1111.111 is NaN): largest finite S.1111.110 = 448, smallest normal
+# S.0001.000 = 2^-6, largest subnormal S.0000.111 = 7/8 * 2^-6, smallest subnormal 2^-9.
+
+E4M3_SPEC = [(448.0, 0x7E), (-448.0, 0xFE), (1.0, 0x38), (-1.0, 0xB8), (0.5, 0x30),
+             (2.0 ** -6, 0x08), (7 * 2.0 ** -9, 0x07), (2.0 ** -9, 0x01), (256.0, 0x78),
+             (1.125, 0x39), (240.0, 0x77), (0.0, 0x00), (-0.0, 0x80)]
+
+
+@pytest.mark.parametrize("v,code", E4M3_SPEC)
+def test_e4m3_spec_values(v, code):
+    assert oracle.e4m3_encode(v) == code
+    assert oracle.e4m3_decode(code) == v and math.copysign(1, oracle.e4m3_decode(code)) == math.copysign(1, v)
+
+
+def test_e4m3_rounding_saturation_and_nan():
+    # ties to even at the subnormal end: 2^-10 is half of the smallest subnormal
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00
+    assert oracle.e4m3_encode(-(2.0 ** -10)) == 0x80
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02      # 1.5 quanta -> 2 (even)
+    assert oracle.e4m3_encode(5 * 2.0 ** -10) == 0x02      # 2.5 quanta -> 2 (even)
+    assert oracle.e4m3_encode(1.0625) == 0x38               # halfway 1 and 1.125 -> even (1)
+    assert oracle.e4m3_encode(1.1875) == 0x3A               # halfway 1.125 and 1.25 -> 1.25
+    # beyond the largest finite value: saturate, never NaN
+    for v in (448.0001, 464.0, 480.0, 1e9, float("inf")):
+        assert oracle.e4m3_encode(v) == 0x7E and oracle.e4m3_encode(-v) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_round_trip_and_nearest_even_brute_force():
+    finite = [b for b in range(256) if b not in (0x7F, 0xFF)]
+    for b in finite:
+        assert oracle.e4m3_encode(oracle.e4m3_decode(b)) == b
+    pos = sorted((oracle.e4m3_decode(b), b) for b in range(0x00, 0x7F))
+    for (va, ba), (vb, bb) in zip(pos, pos[1:]):
+        mid = (va + vb) / 2
+        assert oracle.e4m3_encode(mid) == (ba if ba % 2 == 0 else bb)     # tie -> even code
+        assert oracle.e4m3_encode(va + (vb - va) * 0.25) == ba
+        assert oracle.e4m3_encode(va + (vb - va) * 0.75) == bb
+
+
+@pytest.mark.parametrize("amax,e_floor,e_ceil", [
+    (1.0, -8, -8), (1.75, -8, -8), (1.875, -8, -7), (448.0, 0, 0), (449.0, 0, 1),
+    (2.0 ** -20, -28, -28), (3 * 2.0 ** 100, 93, 93), (3.75 * 2.0 ** 100, 93, 94)])
+def test_mx_scale_exponent(amax, e_floor, e_ceil):
+    # mode 0: E = floor(log2 amax) - 8; mode 1: smallest E with amax <= 448 * 2^E
+    assert oracle.mx_scale_exp(amax, 0) == e_floor
+    assert oracle.mx_scale_exp(amax, 1) == e_ceil
+    assert amax <= 448 * 2.0 ** e_ceil and amax > 448 * 2.0 ** (e_ceil - 1)
+    assert 2.0 ** (e_floor + 8) <= amax < 2.0 ** (e_floor + 9)
+
+
+def test_mx_scale_exponent_zero_and_clamp():
+    assert oracle.mx_scale_exp(0.0, 0) == -127 and oracle.mx_scale_exp(0.0, 1) == -127
+    assert oracle.mx_scale_exp(2.0 ** -133, 0) == -127     # bf16's smallest subnormal
+
+
+def test_mx_scale_tile_layout_is_a_bijection_with_contiguous_rows():
+    T, H = 300, 7168 + 32 * 5                    # ragged rows and block columns
+    rows, cols = oracle.mx_scale_shape(T, H)
+    assert rows == 384 and cols == (H // 32 + 3) // 4 * 4
+    seen = np.zeros(rows * cols, np.int32)
+    for m in range(rows):
+        for k in range(cols):
+            seen[oracle.mx_scale_offset(m, k, H)] += 1
+    assert np.all(seen == 1)
+    # four consecutive blocks of one token are four consecutive bytes; tokens m and m + 32 of a
+    # 128-row tile sit 4 bytes apart; each 128 x 4 tile is 512 contiguous bytes
+    for m in (0, 37, 127, 255):
+        base = oracle.mx_scale_offset(m, 8, H)
+        assert [oracle.mx_scale_offset(m, 8 + j, H) for j in range(4)] == [base + j for j in range(4)]
+    assert oracle.mx_scale_offset(32, 0, H) - oracle.mx_scale_offset(0, 0, H) == 4
+    assert oracle.mx_scale_offset(1, 0, H) - oracle.mx_scale_offset(0, 0, H) == 16
+    assert oracle.mx_scale_offset(0, 4, H) - oracle.mx_scale_offset(0, 0, H) == 512
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mxfp8_quantize_decodes_back_within_half_a_quantum(mode):
+    rng = np.random.default_rng(11)
+    T, H = 5, 256
+    mag = 10.0 ** rng.uniform(-3, 3, size=(T, H // 32, 1))
+    X = bf(rng.standard_normal((T, H // 32, 32)) * mag).reshape(T, H)
+    q, sc = oracle.mxfp8_quantize(X, mode)
+    x = F(X).astype(np.float64)
+    for t in range(T):
+        for k in range(H // 32):
+            blk = x[t, 32 * k:32 * k + 32]
+            E = int(sc[oracle.mx_scale_offset(t, k, H)]) - 127
+            assert E == oracle.mx_scale_exp(np.abs(blk).max(), mode)
+            scaled = np.abs(blk) / 2.0 ** E
+            if mode == 1:
+                assert scaled.max() <= 448
+            else:
+                assert 256 <= scaled.max() < 512
+            dec = np.array([oracle.e4m3_decode(b) for b in q[t, 32 * k:32 * k + 32]]) * 2.0 ** E
+            for xv, dv, sv in zip(blk, dec, scaled):
+                if sv > 448:
+                    assert dv == math.copysign(448 * 2.0 ** E, xv)     # saturated
+                    continue
+                be = max(math.floor(math.log2(sv)) if sv > 0 else -6, -6)
+                assert abs(dv - xv) <= 2.0 ** (E + be - 4) * (1 + 1e-12)   # half a quantum
