@@ -137,6 +137,44 @@ MHC_API mhc_status mhc_shifted_post_pre(
     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/* MXFP8 block-scale rules for the quantized layer input (the pages name MXFP8 and the
+ * UE8M0 scale byte but give no formula; both rules are offered). */
+typedef enum mhc_mx_scale_mode {
+    MHC_MX_SCALE_FLOOR = 0,  /* E = floor(log2 amax) - 8 (OCP MX): the largest element lands in
+                                [256, 512) and saturates to 448 above 448 */
+    MHC_MX_SCALE_CEIL = 1    /* the smallest E with amax <= 448 * 2^E: no element saturates */
+} mhc_mx_scale_mode;
+
+/* Bytes of the layer input's MXFP8 scale block for T tokens of size H (H % 32 == 0;
+ * 0 otherwise): (T rounded up to 128) * (H / 32 rounded up to 4). */
+MHC_API size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H);
+
+/* The fused step (1)-(4) with the layer input also emitted as MXFP8, the quantize that
+ * consumes it fused into the combine+RMSNorm epilogue ("[DSV4.1] Four BS=1 critical-path
+ * fixes for DSpark decode", "What changed" item 3 and "Correctness").  Arguments and the other
+ * outputs as in mhc_shifted_post_pre, plus:
+ *   layer_in_out      [T,H] bf16, or NULL to skip the bf16 layer input
+ *   layer_in_fp8      [T,H] uint8  E4M3 codes of x / 2^E for each block of 32 consecutive
+ *                     values of a token (x = the bf16 layer input; round to nearest even,
+ *                     finite values beyond 448 saturate); 16-byte aligned
+ *   layer_in_scales   mhc_mxfp8_scale_bytes(T, H) bytes: the byte E + 127 of block k of
+ *                     token m at ((m/128)*KT + k/4)*512 + (m%32)*16 + ((m%128)/32)*4 + k%4,
+ *                     KT = ceil(H/128) (the 128x4 tile layout of block-scaled tensor-core
+ *                     GEMMs); padding bytes (m >= T, k >= H/32) are not written
+ *   scale_mode        MHC_MX_SCALE_FLOOR or MHC_MX_SCALE_CEIL; E is clamped to [-127, 127],
+ *                     and an all-zero block gets E = -127
+ * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  Runs on the ws and small schedules
+ * (AUTO picks one of them); a forced other schedule returns MHC_ERR_UNSUPPORTED.  The bf16
+ * output and the mixes are bit-identical to mhc_shifted_post_pre's on the same schedule. */
+MHC_API mhc_status mhc_shifted_post_pre_mxfp8(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,
+    const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps,
+    float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, uint8_t *layer_in_fp8, uint8_t *layer_in_scales, int scale_mode,
+    float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out, void *workspace,
+    size_t workspace_bytes, void *stream);
+
 /* The fused step (1)-(4) for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point.
  * Some callers cannot call cudaMalloc where they run the op: a host framework

@@ -19,7 +19,9 @@ from . import _build
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
+    "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL",
 ]
+MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
 OK = 0
 STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
@@ -53,6 +55,11 @@ def lib():
             L.mhc_shifted_post_pre.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
                                                P, P, P, P, P, P, Z, P]
             L.mhc_shifted_post_pre.restype = I
+            L.mhc_shifted_post_pre_mxfp8.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
+                                                     P, P, P, P, I, P, P, P, P, Z, P]
+            L.mhc_shifted_post_pre_mxfp8.restype = I
+            L.mhc_mxfp8_scale_bytes.argtypes = [I64, I64]
+            L.mhc_mxfp8_scale_bytes.restype = Z
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -159,6 +166,42 @@ def shifted_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi,
         _ptr(o["pre_mix"]), _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream, dev))
     _check(rc, "mhc_shifted_post_pre")
+    return o
+
+
+def mxfp8_scale_bytes(T: int, H: int) -> int:
+    return int(lib().mhc_mxfp8_scale_bytes(int(T), int(H)))
+
+
+def shifted_post_pre_mxfp8(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                           rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                           sinkhorn_iters=20, scale_mode=MX_SCALE_FLOOR, want_bf16=True, out=None,
+                           workspace=None, stream=None):
+    """mhc_shifted_post_pre_mxfp8: the fused step with the layer input also as MXFP8.  Returns the
+    dict of shifted_post_pre (layer_in only if want_bf16) plus layer_in_fp8 [T,H] uint8 (E4M3
+    codes) and layer_in_scales (uint8, mxfp8_scale_bytes(T, H), 128x4 tile layout)."""
+    torch = _torch()
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
+    _bf16(rmsnorm_weight, "rmsnorm_weight", (H,))
+    dev = residual.device
+    o = dict(out or {})
+    if not want_bf16:
+        o.setdefault("layer_in", None)
+    o = _outputs(T, H, dev, o, True)
+    o.setdefault("layer_in_fp8", torch.empty((T, H), dtype=torch.uint8, device=dev))
+    o.setdefault("layer_in_scales", torch.empty(max(mxfp8_scale_bytes(T, H), 1), dtype=torch.uint8, device=dev))
+    ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    rc = lib().mhc_shifted_post_pre_mxfp8(
+        _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
+        _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
+        hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
+        _ptr(o["layer_in_fp8"]), _ptr(o["layer_in_scales"]), int(scale_mode), _ptr(o["pre_mix"]),
+        _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream, dev))
+    _check(rc, "mhc_shifted_post_pre_mxfp8")
     return o
 
 

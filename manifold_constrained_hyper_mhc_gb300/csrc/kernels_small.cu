@@ -161,14 +161,14 @@ __device__ __forceinline__ float4 warp_cta_sum16(const float *src, int stride, i
     return a;
 }
 
-template <bool kPost>
+template <bool kPost, bool kMx>
 __global__ void __launch_bounds__(kSNT, 1)
 small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, const float *__restrict__ prev_post,
              const float *__restrict__ prev_comb, const float *__restrict__ phi, const float *__restrict__ bias,
              const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int T, int H,
              int Hs, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
              float *__restrict__ post_out, float *__restrict__ res_out, float *__restrict__ part,
-             unsigned int *__restrict__ ctrl) {
+             unsigned int *__restrict__ ctrl, MxOut mx) {
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, nc = gridDim.x;
@@ -452,19 +452,27 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
     wsync();
     if (owner_cta) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums and stats -> owner warp
 
-    // ---- 5. combine + RMSNorm of the slice
-    for (int item = wt; item < T * nvec; item += nwork) {
+    // ---- 5. combine + RMSNorm of the slice.  Warp-uniform loop: with the MXFP8 output, the four
+    // lanes 4a .. 4a+3 hold one block of 32 (nvec is then a multiple of 4).
+    for (int base = wt - lane; base < T * nvec; base += nwork) {
+        const int item = base + lane;
         const int t = item / nvec, v = item % nvec;
-        if (v * kVec >= hv) continue;
-        const float4 p4 = *reinterpret_cast<const float4 *>(sSt + t * 8);
-        const float pre[kHC] = {p4.x, p4.y, p4.z, p4.w};
-        float rf[kHC][8], x[8];
+        const bool act = item < T * nvec && v * kVec < hv;
+        uint4 ob = make_uint4(0u, 0u, 0u, 0u);
+        if (act) {
+            const float4 p4 = *reinterpret_cast<const float4 *>(sSt + t * 8);
+            const float pre[kHC] = {p4.x, p4.y, p4.z, p4.w};
+            float rf[kHC][8], x[8];
 #pragma unroll
-        for (int j = 0; j < kHC; ++j)
-            unpack8(*reinterpret_cast<const uint4 *>(sRp + (size_t)t * RS + j * Hs + v * kVec), rf[j]);
-        combine_vec8_x2(rf, pre, x);
-        st_stream(X_out + (size_t)t * H + h0 + v * kVec,
-                  norm_vec8(x, sSt[t * 8 + 4], *reinterpret_cast<const uint4 *>(sGam + v * kVec)));
+            for (int j = 0; j < kHC; ++j)
+                unpack8(*reinterpret_cast<const uint4 *>(sRp + (size_t)t * RS + j * Hs + v * kVec), rf[j]);
+            combine_vec8_x2(rf, pre, x);
+            ob = norm_vec8(x, sSt[t * 8 + 4], *reinterpret_cast<const uint4 *>(sGam + v * kVec));
+            if (!kMx || X_out != nullptr) st_stream(X_out + (size_t)t * H + h0 + v * kVec, ob);
+        }
+        if (kMx)
+            mx_quantize8(ob, act, mx.mode, mx.q + (size_t)t * H + h0 + v * kVec,
+                         mx.scale + mx_scale_offset(t, (h0 + v * kVec) / 32, H));
     }
     if (dead && wt == 0) atomicOr(ctrl, 1u);
 }
@@ -475,13 +483,13 @@ int small_ctas(int H, int num_sms) {
     const int n = (H + 63) / 64;
     return n < num_sms ? n : num_sms;
 }
-int small_slice(int H, int num_sms) {
+int small_slice(int H, int num_sms, int align) {
     const int n = small_ctas(H, num_sms);
-    return ((H + n - 1) / n + 7) / 8 * 8;
+    return ((H + n - 1) / n + align - 1) / align * align;
 }
-bool small_supported(int64_t T, int H, int num_sms) {
+bool small_supported(int64_t T, int H, int num_sms, bool mx) {
     if (T < 1 || T > kSmallMaxT || num_sms < 1) return false;
-    const int Hs = small_slice(H, num_sms);
+    const int Hs = small_slice(H, num_sms, mx ? 32 : 8);
     const int n = (H + Hs - 1) / Hs;
     if (n > kMaxCtas) return false;
     return SmallSmem{(int)T, Hs, n}.bytes() <= kSmallSmemLimit;
@@ -492,11 +500,13 @@ size_t small_workspace_bytes(int64_t T, int H) {
 }
 
 cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream) {
-    if (!small_supported(a.T, a.H, num_sms)) return cudaErrorInvalidValue;
-    const int Hs = small_slice(a.H, num_sms);
+    const bool mxo = a.mx.q != nullptr;
+    if (!small_supported(a.T, a.H, num_sms, mxo)) return cudaErrorInvalidValue;
+    const int Hs = small_slice(a.H, num_sms, mxo ? 32 : 8);  // MXFP8: slices hold whole blocks of 32
     const int n = (a.H + Hs - 1) / Hs;  // every CTA holds at least one vector of the slice
     const bool post = a.R_out != nullptr;
-    auto kern = post ? small_kernel<true> : small_kernel<false>;
+    auto kern = post ? (mxo ? small_kernel<true, true> : small_kernel<true, false>)
+                     : (mxo ? small_kernel<false, true> : small_kernel<false, false>);
     const size_t smem = SmallSmem{(int)a.T, Hs, n}.bytes();
     cudaError_t e;
     if (smem > 48 * 1024 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
@@ -514,7 +524,7 @@ cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cu
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.bias, a.mix_scales, a.gamma,
                               a.s, (int)a.T, a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, a.part,
-                              ctrl);
+                              ctrl, a.mx);
 }
 
 }  // namespace mhc

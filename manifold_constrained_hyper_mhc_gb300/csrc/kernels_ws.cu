@@ -181,13 +181,13 @@ struct WsMaps {
     CUtensorMap R, Y, comb, post;
 };
 
-template <bool kPost>
+template <bool kPost, bool kMx>
 __global__ void __launch_bounds__(kNT, 1)
 ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pack, const float *__restrict__ bias,
           const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H,
           int Hs, RLayout lay, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out,
           float *__restrict__ pre_out, float *__restrict__ post_out, float *__restrict__ res_out,
-          float *__restrict__ zstash, unsigned int *__restrict__ status) {
+          float *__restrict__ zstash, unsigned int *__restrict__ status, MxOut mx) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzled TMA boxes need a 1024-byte aligned base (1 KB of slack is allocated)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -510,14 +510,20 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             const bool tok_ok = t0 + c_tok < T;
 #pragma unroll
             for (int k = 0; k < kCItems; ++k) {
-                if (c_on[k] && tok_ok) {
+                const bool act = c_on[k] && tok_ok;
+                uint4 ob = make_uint4(0u, 0u, 0u, 0u);
+                if (act) {
                     const unsigned char *rp = rb + c_roff[k];
                     float rf[kHC][8], x[8];
 #pragma unroll
                     for (int j = 0; j < kHC; ++j) unpack8(*reinterpret_cast<const uint4 *>(rp + j * lay.s_j), rf[j]);
                     combine_vec8_x2(rf, pre, x);
-                    st_stream(xrow + c_xoff[k], norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16)));
+                    ob = norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16));
+                    if (!kMx || X_out != nullptr) st_stream(xrow + c_xoff[k], ob);
                 }
+                if (kMx)  // blocks of 32 = four consecutive vectors = lanes 4a .. 4a+3 of one token
+                    mx_quantize8(ob, act, mx.mode, mx.q + t0 * (int64_t)H + c_xoff[k],
+                                 mx.scale + mx_scale_offset(t0 + c_tok, (h0 + c_v[k] * kVec) / 32, H));
             }
             // every use of the slot (post, projection, combine) is over: refill it with group q + kNBuf
             fence_proxy_async_smem();
@@ -799,12 +805,14 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     launch_pack_phi(a.phi, a.H, kC, Hs, a.phi_pack, total, stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    auto kern = post ? ws_kernel<true> : ws_kernel<false>;
+    const bool mxo = a.mx.q != nullptr;
+    auto kern = post ? (mxo ? ws_kernel<true, true> : ws_kernel<true, false>)
+                     : (mxo ? ws_kernel<false, true> : ws_kernel<false, false>);
     const size_t smem = Layout{Hs / 64}.bytes() + 1024;  // + alignment slack
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    static int max_clusters[64][2];
+    static int max_clusters[64][4];
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -820,7 +828,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     cfg.dynamicSmemBytes = std::max<size_t>(smem, 227 * 1024 / 2 + 1024);
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        int &mc = max_clusters[dev][post ? 1 : 0];
+        int &mc = max_clusters[dev][(post ? 1 : 0) + (mxo ? 2 : 0)];
         if (mc == 0) {
             if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) != cudaSuccess)
                 return e;
@@ -836,7 +844,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
     return cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                              a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status);
+                              a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);
 }
 
 }  // namespace mhc

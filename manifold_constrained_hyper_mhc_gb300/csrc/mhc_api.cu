@@ -136,17 +136,21 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
 // Up to this many tokens the one-barrier small-T schedule has the lower latency.
 constexpr int64_t kSmallAutoMaxT = 32;
 
-int auto_schedule(int64_t T, int64_t H, int sms) {
-    if (T <= kSmallAutoMaxT && mhc::small_supported(T, (int)H, sms)) return MHC_SCHEDULE_SMALL;
+int auto_schedule(int64_t T, int64_t H, int sms, bool mx = false) {
+    if (T <= kSmallAutoMaxT && mhc::small_supported(T, (int)H, sms, mx)) return MHC_SCHEDULE_SMALL;
     if (mhc::ws_supported((int)H)) return MHC_SCHEDULE_WS;
     if (mhc::pipe_supported((int)H)) return MHC_SCHEDULE_PIPE;
     return cluster_fits(kGeomDefault, H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
 }
 
-int choose_schedule(int64_t T, int64_t H, int sms) {
+int choose_schedule(int64_t T, int64_t H, int sms, bool mx) {
     const int forced = g_forced_schedule.load(std::memory_order_relaxed);
     if (forced != MHC_SCHEDULE_AUTO) return forced;
-    return auto_schedule(T, H, sms);
+    return auto_schedule(T, H, sms, mx);
+}
+
+size_t mx_scale_bytes(int64_t T, int64_t H) {
+    return (size_t)((T + 127) / 128 * 128) * (size_t)((H / 32 + 3) / 4 * 4);
 }
 
 // Common body of the fused call (post != nullptr) and the pre-only call.
@@ -157,18 +161,28 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                         float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps,
                         int sinkhorn_iters, mhc_bf16 *residual_out, mhc_bf16 *layer_in_out,
                         float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
-                        void *workspace, size_t workspace_bytes, void *stream, bool fused) {
+                        void *workspace, size_t workspace_bytes, void *stream, bool fused,
+                        uint8_t *mx_q = nullptr, uint8_t *mx_scale = nullptr, int mx_mode = 0) {
     mhc_status st;
     g_launches = 0;
+    const bool mx = mx_q != nullptr || mx_scale != nullptr;
     if ((st = check_sizes(T, H)) != MHC_OK) return st;
     if ((st = check_scalars(hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters)) != MHC_OK)
         return st;
     if (T == 0) return MHC_OK;
     if ((st = check_ptrs({{residual, "residual"}, {phi, "phi"}, {bias, "bias"},
                           {mix_scales, "mix_scales"}, {rmsnorm_weight, "rmsnorm_weight"},
-                          {layer_in_out, "layer_in_out"}, {pre_mix_out, "pre_mix_out"},
+                          {pre_mix_out, "pre_mix_out"},
                           {post_mix_out, "post_mix_out"}, {comb_res_mix_out, "comb_res_mix_out"}})) != MHC_OK)
         return st;
+    if ((!mx || layer_in_out != nullptr) && (st = check_ptrs({{layer_in_out, "layer_in_out"}})) != MHC_OK) return st;
+    if (mx) {
+        if (H % 32 != 0) return fail(MHC_ERR_INVALID_ARG, "the MXFP8 output needs H %% 32 == 0 (H=%lld)", (long long)H);
+        if (mx_mode != MHC_MX_SCALE_FLOOR && mx_mode != MHC_MX_SCALE_CEIL)
+            return fail(MHC_ERR_INVALID_ARG, "unknown MXFP8 scale mode %d", mx_mode);
+        if ((st = check_ptrs({{mx_q, "layer_in_fp8"}})) != MHC_OK) return st;
+        if (mx_scale == nullptr) return fail(MHC_ERR_INVALID_ARG, "layer_in_scales is NULL");
+    }
     if (fused && (st = check_ptrs({{layer_out, "layer_out"}, {prev_post_mix, "prev_post_mix"},
                                    {prev_comb_res_mix, "prev_comb_res_mix"},
                                    {residual_out, "residual_out"}})) != MHC_OK)
@@ -188,16 +202,17 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
     const Span ins[] = {sR, sY, sPP, sPC, sPhi, sB, sMS, sG};
     const Span oRo{fused ? residual_out : nullptr, tok * 4 * H * 2}, oX{layer_in_out, tok * H * 2},
         oPre{pre_mix_out, tok * 16}, oPost{post_mix_out, tok * 16}, oRes{comb_res_mix_out, tok * 64};
-    const Span outs[] = {oRo, oX, oPre, oPost, oRes, sW};
+    const Span oQ{mx_q, mx ? tok * H : 0}, oS{mx_scale, mx ? mx_scale_bytes(T, H) : 0};
+    const Span outs[] = {oRo, oX, oPre, oPost, oRes, sW, oQ, oS};
     const char *out_names[] = {"residual_out", "layer_in_out", "pre_mix_out", "post_mix_out",
-                               "comb_res_mix_out", "workspace"};
-    for (int o = 0; o < 6; ++o) {
+                               "comb_res_mix_out", "workspace", "layer_in_fp8", "layer_in_scales"};
+    for (int o = 0; o < 8; ++o) {
         for (int i = 0; i < 8; ++i) {
             if (o == 0 && i == 0 && residual_out == residual) continue;  // in-place residual update
             if (overlap(outs[o], ins[i]))
                 return fail(MHC_ERR_INVALID_ARG, "%s overlaps an input", out_names[o]);
         }
-        for (int p = o + 1; p < 6; ++p)
+        for (int p = o + 1; p < 8; ++p)
             if (overlap(outs[o], outs[p]))
                 return fail(MHC_ERR_INVALID_ARG, "%s overlaps %s", out_names[o], out_names[p]);
     }
@@ -207,7 +222,10 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
 
     // mix_scales stays a device pointer: the kernels read the three alphas.
     mhc::Scalars s{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
-    const int sched = choose_schedule(T, H, dev.sms);
+    const int sched = choose_schedule(T, H, dev.sms, mx);
+    const mhc::MxOut mxo{mx_q, mx_scale, mx_mode};
+    if (mx && sched != MHC_SCHEDULE_WS && sched != MHC_SCHEDULE_SMALL)
+        return fail(MHC_ERR_UNSUPPORTED, "the MXFP8 output is produced by the ws and small schedules only");
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     switch (sched) {
@@ -294,12 +312,13 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.phi_pack = reinterpret_cast<uint4 *>(ws);
             float *zstash = reinterpret_cast<float *>(ws + ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)));
             a.C = 16; a.G = 8;
+            a.mx = mxo;
             e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
             g_launches = 2;
             break;
         }
         case MHC_SCHEDULE_SMALL: {
-            if (!mhc::small_supported(T, (int)H, dev.sms))
+            if (!mhc::small_supported(T, (int)H, dev.sms, mx))
                 return fail(MHC_ERR_UNSUPPORTED, "T=%lld, H=%lld does not fit the small schedule (T <= %d)",
                             (long long)T, (long long)H, mhc::kSmallMaxT);
             mhc::SplitArgs a{};
@@ -310,6 +329,7 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
             a.res_out = comb_res_mix_out;
             a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
+            a.mx = mxo;
             e = mhc::launch_small(a, static_cast<unsigned int *>(workspace), dev.sms, cs);
             g_launches = 1;
             break;
@@ -366,6 +386,29 @@ mhc_status mhc_shifted_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_
                         rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
                         sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
                         comb_res_mix_out, workspace, workspace_bytes, stream, true);
+}
+
+size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H) {
+    if (T < 0 || H < 0 || H % 32 != 0) return 0;
+    return mx_scale_bytes(T, H);
+}
+
+mhc_status mhc_shifted_post_pre_mxfp8(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                                      const float *prev_post_mix, const float *prev_comb_res_mix,
+                                      const float *phi, const float *bias, const float *mix_scales,
+                                      const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
+                                      float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                                      float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+                                      mhc_bf16 *layer_in_out, uint8_t *layer_in_fp8, uint8_t *layer_in_scales,
+                                      int scale_mode, float *pre_mix_out, float *post_mix_out,
+                                      float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+    if (layer_in_fp8 == nullptr && T > 0) return fail(MHC_ERR_INVALID_ARG, "layer_in_fp8 is NULL");
+    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                        comb_res_mix_out, workspace, workspace_bytes, stream, true, layer_in_fp8,
+                        layer_in_scales, scale_mode);
 }
 
 mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const float *bias,

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 
 namespace mhc {
@@ -148,6 +149,58 @@ __device__ __forceinline__ uint4 norm_vec8(const float (&x)[8], float rstd, uint
         o[e + 1] = v.y;
     }
     return pack8_rn(o);
+}
+
+// ---- MXFP8 form of the layer input -----------------------------------------
+// Blocks of 32 consecutive hidden values of a token: E4M3 codes of x / 2^E and the
+// scale byte E + 127, with E from the block's largest magnitude (mode 0:
+// floor(log2 amax) - 8; mode 1: the smallest E with amax <= 448 * 2^E; zero or
+// subnormal amax: -127).  The values quantized are the bf16 outputs.
+struct MxOut {
+    uint8_t *q;      // [T][H] E4M3 codes (nullptr: no MXFP8 output)
+    uint8_t *scale;  // scale bytes in the 128 x 4 tile layout
+    int mode;
+};
+
+__device__ __forceinline__ int mx_exp(float amax, int mode) {
+    const uint32_t u = __float_as_uint(amax);
+    const int ef = (int)((u >> 23) & 0xFFu);
+    if (ef == 0) return -127;
+    int E = ef - 127 - 8;
+    if (mode == 1 && (u & 0x7FFFFFu) > 0x600000u) E += 1;  // significand above 1.75
+    return E < -127 ? -127 : (E > 127 ? 127 : E);
+}
+
+// Byte offset of (token m, block k) in the 128 x 4 tile layout of the scales.
+__device__ __forceinline__ int64_t mx_scale_offset(int64_t m, int k, int H) {
+    const int kt = (H / 32 + 3) / 4;
+    return ((m / 128) * kt + k / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + (k % 4);
+}
+
+// Quantizes the 8 bf16 outputs `o` held by this lane; the four lanes lane ^ 1, lane ^ 2 of
+// an aligned group of four hold one block (consecutive vectors).  Every lane of the warp
+// must call it (inactive lanes with active = false).  Writes the 8 codes at q_dst and, from
+// the group's first lane, the scale byte at scale_dst.
+__device__ __forceinline__ void mx_quantize8(uint4 o, bool active, int mode, uint8_t *q_dst,
+                                             uint8_t *scale_dst) {
+    float x[8];
+    unpack8(o, x);
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    if (!active) amax = 0.f;
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (!active) return;
+    const int E = mx_exp(amax, mode);
+    const float m = __uint_as_float((uint32_t)(127 - E) << 23);  // 2^-E (E <= 120 for finite bf16)
+    uint32_t w[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        w[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x[2 * p] * m, x[2 * p + 1] * m), __NV_SATFINITE,
+                                                   __NV_E4M3);
+    *reinterpret_cast<uint2 *>(q_dst) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    if (((threadIdx.x & 31) & 3) == 0) *scale_dst = (uint8_t)(E + 127);
 }
 
 // ---- step (3): heads and Sinkhorn, one warp per token -----------------------

@@ -30,6 +30,7 @@ struct SplitArgs {
     uint16_t *X_out;
     float *pre_out, *post_out, *res_out;
     float *part;  // workspace: [T][ceil(H/256)][32] floats
+    MxOut mx;     // MXFP8 layer input (mx.q == nullptr: none)
 };
 
 inline size_t split_workspace_bytes(int64_t T, int64_t H) {
@@ -53,6 +54,7 @@ struct FusedArgs {
     float *pre_out, *post_out, *res_out;
     uint4 *phi_pack;  // workspace: fused_pack_bytes(H, C)
     int C, G;         // cluster size, tokens per group
+    MxOut mx;         // MXFP8 layer input (mx.q == nullptr: none); ws and small schedules only
 };
 
 int fused_slice(int H, int C);                     // hidden elements per CTA (multiple of 16)
@@ -92,8 +94,8 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
 // one grid barrier on a 64-bit arrival counter at control-block bytes 64..71.
 constexpr int kSmallMaxT = 64;
 int small_ctas(int H, int num_sms);
-int small_slice(int H, int num_sms);
-bool small_supported(int64_t T, int H, int num_sms);
+int small_slice(int H, int num_sms, int align);  // align 8, or 32 for the MXFP8 output
+bool small_supported(int64_t T, int H, int num_sms, bool mx);
 size_t small_workspace_bytes(int64_t T, int H);  // upper bound over SM counts
 cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream);
 
