@@ -37,11 +37,15 @@ METRIC = "tokens/s and HBM GB/s (% of GB300 peak) for fused mHC post+pre vs T, H
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algorithmic_bytes(T: int, H: int) -> int:
+def algorithmic_bytes(T: int, H: int, mxfp8: bool = False) -> int:
     """Bytes the op must move per call: per token R 8H + Y 2H + prev mixes 80 B in,
     R' 8H + layer input 2H + mixes 96 B out; per call phi 96H + gamma 2H + bias and
-    mix scales 108 B."""
-    return T * (20 * H + 176) + 96 * H + 2 * H + 108
+    mix scales 108 B.  With the MXFP8 layer input: + H E4M3 bytes and H/32 scale bytes
+    per token."""
+    b = T * (20 * H + 176) + 96 * H + 2 * H + 108
+    if mxfp8:
+        b += T * (H + H // 32)
+    return b
 
 
 def peaks():
@@ -213,14 +217,47 @@ def run_ours(args, rank, world, lr, dist):
            "comb_res_mix": torch.empty((T, 4, 4), device=dev)}
     stream = torch.cuda.current_stream(dev)
 
+    mx_mode = {"none": None, "floor": mhc.MX_SCALE_FLOOR, "ceil": mhc.MX_SCALE_CEIL}[args.mxfp8]
+    if mx_mode is not None:
+        out["layer_in_fp8"] = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        out["layer_in_scales"] = torch.empty(mhc.mxfp8_scale_bytes(T, H), dtype=torch.uint8, device=dev)
+
+    def call(R_, Y_, pp_, pc_):
+        if mx_mode is None:
+            mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=out, workspace=ws, stream=stream)
+        else:
+            mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode, out=out, workspace=ws,
+                                       stream=stream)
+
     def step():
-        mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=stream)
+        call(Rd, Yd, ppd, pcd)
 
     for _ in range(max(3, args.warmup)):
         step()
     launches = mhc.last_launch_count()
     torch.cuda.synchronize(dev)
     mhc.check_status(ws)
+    run_steps, n_replay = step, args.steps
+    if args.graph > 0:
+        # launch-bound sizes: capture `graph` calls into one CUDA graph and replay it, so the
+        # timed region measures the device, not the host's per-call launch overhead
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gstream):
+            for _ in range(args.graph):
+                mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=gstream) \
+                    if mx_mode is None else \
+                    mhc.shifted_post_pre_mxfp8(Rd, Yd, ppd, pcd, *wd, **sc, scale_mode=mx_mode, out=out,
+                                               workspace=ws, stream=gstream)
+        n_replay = max(1, args.steps // args.graph)
+        args.steps = n_replay * args.graph
+
+        def run_steps():
+            g.replay()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
 
     def barrier():
         if dist is not None:
@@ -231,13 +268,41 @@ def run_ours(args, rank, world, lr, dist):
     barrier()
     with ClockSampler(dev.index) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for _ in range(n_replay):
+            run_steps()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
     el_ms = ev0.elapsed_time(ev1)
     mhc.check_status(ws)
+    # the main kernel alone (for the roofline): events recorded by the library right around
+    # its launch, one pair per call, over a separate run of calls
+    nk = max(3, min(args.steps, 200))
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+    for a_, b_ in kev:  # torch creates the CUDA event on its first record
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    if args.graph > 0:  # the event pairs recorded inside a captured graph, replayed once
+        kg = torch.cuda.CUDAGraph()
+        gstream2 = torch.cuda.Stream(dev)
+        gstream2.wait_stream(stream)
+        with torch.cuda.graph(kg, stream=gstream2):
+            for a_, b_ in kev:
+                mhc.set_main_kernel_events(a_, b_)
+                mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=gstream2) \
+                    if mx_mode is None else \
+                    mhc.shifted_post_pre_mxfp8(Rd, Yd, ppd, pcd, *wd, **sc, scale_mode=mx_mode, out=out,
+                                               workspace=ws, stream=gstream2)
+            mhc.set_main_kernel_events(None, None)
+        kg.replay()
+    else:
+        for a_, b_ in kev:
+            mhc.set_main_kernel_events(a_, b_)
+            step()
+        mhc.set_main_kernel_events(None, None)
+    torch.cuda.synchronize(dev)
+    kernel_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in kev]))
     if dist is not None:
         t = torch.tensor([el_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -261,7 +326,7 @@ def run_ours(args, rank, world, lr, dist):
         bufY.view(torch.int16).copy_(hY, non_blocking=True)
         bufpp.copy_(hpp, non_blocking=True)
         bufpc.copy_(hpc, non_blocking=True)
-        mhc.shifted_post_pre(bufR, bufY, bufpp, bufpc, *wd, **sc, out=out, workspace=ws, stream=stream)
+        call(bufR, bufY, bufpp, bufpc)
         for k, v in out.items():
             hout[k].copy_(v, non_blocking=True)
 
@@ -284,21 +349,25 @@ def run_ours(args, rank, world, lr, dist):
     if rank != 0:
         return
     peak, peak_src = peaks()
-    abytes = algorithmic_bytes(T, H)
-    achieved = abytes / (ms_step / 1e3) / 1e9
+    abytes = algorithmic_bytes(T, H, mx_mode is not None)
+    achieved = abytes / (kernel_ms / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
         {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H, "io": "bf16 streams, fp32 mixes",
+        "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H,
+                   "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)"),
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
-                   "hbm_gbs": achieved, "hbm_frac": achieved / peak},
+                   "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": measured_traffic(sched, w.name, T, H), "peak_source": peak_src,
-                     "kernel": f"whole call ({launches} launches), algorithmic bytes {abytes}"},
+                     "traffic": measured_traffic(sched if mx_mode is None else sched + "_mxfp8", w.name, T, H), "peak_source": peak_src,
+                     "kernel": f"main kernel of the call ({launches} launches per call), "
+                               f"{kernel_ms * 1e3:.1f} us per launch (CUDA events around it, {nk} launches), "
+                               f"algorithmic bytes {abytes} per launch"},
         "gpu_launches": launches * args.steps,
+        "launch_mode": f"CUDA graph of {args.graph} calls, replayed" if args.graph > 0 else "eager",
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clk.summary(),
@@ -321,6 +390,10 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")
+    ap.add_argument("--mxfp8", default="none", choices=["none", "floor", "ceil"],
+                    help="also emit the layer input as MXFP8 (E4M3 + UE8M0 block scales)")
     args = ap.parse_args()
     rank, world, lr, dist = dist_setup()
     try:

@@ -236,6 +236,13 @@ MHC_API mhc_status mhc_check_status(void *workspace, void *stream);
  * or launched nothing). */
 MHC_API int mhc_last_launch_count(void);
 
+/* Measurement hook: while set (non-NULL cudaEvent_t handles, passed as void*), every call
+ * on this thread records `start` on its stream right before the launch of its main kernel
+ * and `stop` right after it (for the ws schedule that excludes the phi packing launch), so
+ * cudaEventElapsedTime(start, stop) is that kernel's duration.  Inside a stream capture the
+ * records become event-record nodes of the graph.  NULL, NULL turns it off. */
+MHC_API void mhc_set_main_kernel_events(void *start, void *stop);
+
 /* Static description of a status code; never NULL. */
 MHC_API const char *mhc_status_string(int status);
 

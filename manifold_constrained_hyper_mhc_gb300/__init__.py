@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
-    "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL",
+    "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
 ]
 MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
@@ -74,6 +74,8 @@ def lib():
             L.mhc_status_string.restype = ctypes.c_char_p
             L.mhc_last_launch_count.argtypes = []
             L.mhc_last_launch_count.restype = I
+            L.mhc_set_main_kernel_events.argtypes = [P, P]
+            L.mhc_set_main_kernel_events.restype = None
             L.mhc_last_error.argtypes = []
             L.mhc_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -250,6 +252,13 @@ def auto_schedule(T: int, H: int) -> int:
 def last_launch_count() -> int:
     """Kernels launched by the last library call on this thread."""
     return int(lib().mhc_last_launch_count())
+
+
+def set_main_kernel_events(start=None, stop=None):
+    """Measurement hook: record these torch.cuda.Event objects around each call's main kernel
+    (None, None turns it off)."""
+    lib().mhc_set_main_kernel_events(None if start is None else ctypes.c_void_p(start.cuda_event),
+                                     None if stop is None else ctypes.c_void_p(stop.cuda_event))
 
 
 def check_status(workspace, stream=None):

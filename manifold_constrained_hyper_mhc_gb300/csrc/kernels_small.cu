@@ -522,9 +522,12 @@ cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cu
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.bias, a.mix_scales, a.gamma,
-                              a.s, (int)a.T, a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, a.part,
-                              ctrl, a.mx);
+    mark_main_kernel(stream, true);
+    e = cudaLaunchKernelEx(&cfg, kern, a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.bias, a.mix_scales, a.gamma,
+                           a.s, (int)a.T, a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, a.part,
+                           ctrl, a.mx);
+    mark_main_kernel(stream, false);
+    return e;
 }
 
 }  // namespace mhc

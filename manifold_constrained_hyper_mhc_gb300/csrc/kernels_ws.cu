@@ -481,20 +481,28 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         if (lane == 0)
             for (int q = 0; q < kNBuf && q < n_it; ++q) issue(q);
         // token-major items: thread ct works on token ct / kCPT, vectors ct % kCPT + kCPT * k, so the
-        // token's (pre, rstd) is read once per group; offsets computed once
+        // token's (pre, rstd) is read once per group; offsets computed once.  With the MXFP8 output
+        // the thread instead takes the four vectors of block b = ct % kCPT (at most 14 blocks of
+        // 32 in a slice), vector j = (k + b / 2) % 4 of it at step k: the 16-byte chunks read by
+        // lanes 0-7 (and 8-15) of one token then all differ, so the loads stay conflict-free, and
+        // the block's scale needs no data from other lanes.
         constexpr int kCPT = kStride / kG;  // threads per token (16)
+        static_assert(!kMx || kCItems == 4, "one block of four vectors per thread");
         const int c_tok = ct / kCPT;
         uint32_t c_roff[kCItems];
-        int c_xoff[kCItems], c_v[kCItems];
+        int c_xoff[kCItems], c_v[kCItems], c_j[kCItems];
         bool c_on[kCItems];
 #pragma unroll
         for (int k = 0; k < kCItems; ++k) {
-            const int v = ct % kCPT + kCPT * k;
+            const int b = ct % kCPT;
+            c_j[k] = (k + (b >> 1)) & 3;
+            const int v = kMx ? 4 * b + c_j[k] : ct % kCPT + kCPT * k;
             c_on[k] = v < nvec && h0 + v * kVec < H;
             c_v[k] = v;
             c_roff[k] = r_swz(v >> 3, c_tok, 0, v & 7, lay);
             c_xoff[k] = c_tok * H + h0 + v * kVec;
         }
+        const int c_scol = kMx ? mx_scale_col((h0 + (ct % kCPT) * 32) / 32) : 0;
         for (int q = 0; q < n_it; ++q) {
             const int b = q % kNBuf, s = q % kNPre;
             bwait(&rdy[b], (uint32_t)((q / kNBuf) & 1), dead);
@@ -508,27 +516,28 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             const float rstd = pin[c_tok * 8 + 4];
             const float pre[kHC] = {pr.x, pr.y, pr.z, pr.w};
             const bool tok_ok = t0 + c_tok < T;
+            uint8_t *const srow = kMx ? mx.scale + mx_scale_row(t0 + c_tok, H) : nullptr;
+            uint8_t *const qrow = kMx ? mx.q + t0 * (int64_t)H : nullptr;
+            uint4 ob[kCItems];
 #pragma unroll
             for (int k = 0; k < kCItems; ++k) {
-                const bool act = c_on[k] && tok_ok;
-                uint4 ob = make_uint4(0u, 0u, 0u, 0u);
-                if (act) {
+                ob[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (c_on[k] && tok_ok) {
                     const unsigned char *rp = rb + c_roff[k];
                     float rf[kHC][8], x[8];
 #pragma unroll
                     for (int j = 0; j < kHC; ++j) unpack8(*reinterpret_cast<const uint4 *>(rp + j * lay.s_j), rf[j]);
                     combine_vec8_x2(rf, pre, x);
-                    ob = norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16));
-                    if (!kMx || X_out != nullptr) st_stream(xrow + c_xoff[k], ob);
+                    ob[k] = norm_vec8(x, rstd, *reinterpret_cast<const uint4 *>(sGam + c_v[k] * 16));
+                    if (!kMx || X_out != nullptr) st_stream(xrow + c_xoff[k], ob[k]);
                 }
-                if (kMx)  // blocks of 32 = four consecutive vectors = lanes 4a .. 4a+3 of one token
-                    mx_quantize8(ob, act, mx.mode, mx.q + t0 * (int64_t)H + c_xoff[k],
-                                 mx.scale + mx_scale_offset(t0 + c_tok, (h0 + c_v[k] * kVec) / 32, H));
             }
             // every use of the slot (post, projection, combine) is over: refill it with group q + kNBuf
             fence_proxy_async_smem();
             named_sync(3, kCB * 32);
             if (lane == 0 && q + kNBuf < n_it && !dead) issue(q + kNBuf);
+            if (kMx && c_on[0] && tok_ok)  // from registers, after the refill; the block is in range or not as a whole
+                mx_quantize_block(ob, c_j, mx.mode, qrow + c_xoff[0] - 8 * c_j[0], srow + c_scol);
         }
         if (lane == 0 && cw == 0) {
             // the copies of the last groups issued have landed (already true unless a wait timed out)
@@ -843,8 +852,11 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         }
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
-    return cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                              a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);
+    mark_main_kernel(stream, true);
+    e = cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
+                           a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);
+    mark_main_kernel(stream, false);
+    return e;
 }
 
 }  // namespace mhc

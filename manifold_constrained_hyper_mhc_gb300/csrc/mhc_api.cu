@@ -364,6 +364,20 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
 
 namespace mhc {
 void set_last_error(const char *msg) { g_last_error = msg; }
+
+namespace {
+thread_local cudaEvent_t g_kev_start = nullptr, g_kev_stop = nullptr;
+}
+void mark_main_kernel(cudaStream_t stream, bool start) {
+    cudaEvent_t ev = start ? g_kev_start : g_kev_stop;
+    if (ev == nullptr) return;
+    // inside a stream capture only an external record becomes a record node of the graph
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, stream);
+}
 }  // namespace mhc
 
 extern "C" {
@@ -498,5 +512,10 @@ const char *mhc_status_string(int status) {
 const char *mhc_last_error(void) { return g_last_error.c_str(); }
 
 int mhc_last_launch_count(void) { return g_launches; }
+
+void mhc_set_main_kernel_events(void *start, void *stop) {
+    mhc::g_kev_start = static_cast<cudaEvent_t>(start);
+    mhc::g_kev_stop = static_cast<cudaEvent_t>(stop);
+}
 
 }  // extern "C"

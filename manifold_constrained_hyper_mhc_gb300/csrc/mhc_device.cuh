@@ -171,10 +171,15 @@ __device__ __forceinline__ int mx_exp(float amax, int mode) {
     return E < -127 ? -127 : (E > 127 ? 127 : E);
 }
 
-// Byte offset of (token m, block k) in the 128 x 4 tile layout of the scales.
-__device__ __forceinline__ int64_t mx_scale_offset(int64_t m, int k, int H) {
+// Byte offset of (token m, block k) in the 128 x 4 tile layout of the scales, as the sum of
+// a token part and a block part.
+__device__ __forceinline__ int64_t mx_scale_row(int64_t m, int H) {
     const int kt = (H / 32 + 3) / 4;
-    return ((m / 128) * kt + k / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + (k % 4);
+    return (m / 128) * kt * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4;
+}
+__device__ __forceinline__ int mx_scale_col(int k) { return (k / 4) * 512 + (k % 4); }
+__device__ __forceinline__ int64_t mx_scale_offset(int64_t m, int k, int H) {
+    return mx_scale_row(m, H) + mx_scale_col(k);
 }
 
 // Quantizes the 8 bf16 outputs `o` held by this lane; the four lanes lane ^ 1, lane ^ 2 of
@@ -194,13 +199,41 @@ __device__ __forceinline__ void mx_quantize8(uint4 o, bool active, int mode, uin
     if (!active) return;
     const int E = mx_exp(amax, mode);
     const float m = __uint_as_float((uint32_t)(127 - E) << 23);  // 2^-E (E <= 120 for finite bf16)
+    const float2 m2 = make_float2(m, m);
     uint32_t w[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
-        w[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x[2 * p] * m, x[2 * p + 1] * m), __NV_SATFINITE,
-                                                   __NV_E4M3);
-    *reinterpret_cast<uint2 *>(q_dst) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+    for (int p = 0; p < 4; ++p)  // exact products (a power of two), then one rounding to E4M3
+        w[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(__fmul2_rn(make_float2(x[2 * p], x[2 * p + 1]), m2),
+                                                   __NV_SATFINITE, __NV_E4M3);
+    __stcs(reinterpret_cast<uint2 *>(q_dst), make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
     if (((threadIdx.x & 31) & 3) == 0) *scale_dst = (uint8_t)(E + 127);
+}
+
+// One block of 32 held by one lane as four vectors o[k] (vector j[k] of the block, any
+// order): E4M3 codes to q_block + 8 * j[k], scale byte to *scale_dst.
+__device__ __forceinline__ void mx_quantize_block(const uint4 (&o)[4], const int (&j)[4], int mode,
+                                                  uint8_t *q_block, uint8_t *scale_dst) {
+    float x[4][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        unpack8(o[k], x[k]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[k][e]));
+    }
+    const int E = mx_exp(amax, mode);
+    const float m = __uint_as_float((uint32_t)(127 - E) << 23);  // 2^-E (E <= 120 for finite bf16)
+    const float2 m2 = make_float2(m, m);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            w[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(__fmul2_rn(make_float2(x[k][2 * p], x[k][2 * p + 1]), m2),
+                                                       __NV_SATFINITE, __NV_E4M3);
+        __stcs(reinterpret_cast<uint2 *>(q_block + 8 * j[k]), make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
+    }
+    *scale_dst = (uint8_t)(E + 127);
 }
 
 // ---- step (3): heads and Sinkhorn, one warp per token -----------------------

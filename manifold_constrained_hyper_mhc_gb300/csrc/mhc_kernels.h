@@ -99,6 +99,10 @@ bool small_supported(int64_t T, int H, int num_sms, bool mx);
 size_t small_workspace_bytes(int64_t T, int H);  // upper bound over SM counts
 cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream);
 
+// Records the events set by mhc_set_main_kernel_events (if any) on `stream` right before
+// (start) and after (stop) the launch of a call's main kernel.
+void mark_main_kernel(cudaStream_t stream, bool start);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
