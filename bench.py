@@ -39,10 +39,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 def algorithmic_bytes(T: int, H: int, mxfp8: bool = False) -> int:
     """Bytes the op must move per call: per token R 8H + Y 2H + prev mixes 80 B in,
-    R' 8H + layer input 2H + mixes 96 B out; per call phi 96H + gamma 2H + bias and
-    mix scales 108 B.  With the MXFP8 layer input: + H E4M3 bytes and H/32 scale bytes
-    per token."""
-    b = T * (20 * H + 176) + 96 * H + 2 * H + 108
+    R' 8H + layer input 2H + mixes 96 B out; per call phi (fp32 [4H, 24]) 384H + gamma 2H
+    + bias and mix scales 108 B.  With the MXFP8 layer input: + H E4M3 bytes and H/32 scale
+    bytes per token."""
+    b = T * (20 * H + 176) + 384 * H + 2 * H + 108
     if mxfp8:
         b += T * (H + H // 32)
     return b
