@@ -68,6 +68,8 @@ def _load():
             lib.oracle_mx_scale_offset.restype = I64
             lib.oracle_mxfp8_quantize.argtypes = [P, I64, I64, I, P, P]
             lib.oracle_mxfp8_quantize.restype = I
+            lib.oracle_post_ex.argtypes = [P, P, P, P, P, P, I64, I64, P, P]
+            lib.oracle_post_ex.restype = I
             _lib = lib
     return _lib
 
@@ -201,3 +203,22 @@ def mxfp8_quantize(X, mode: int):
     rc = _load().oracle_mxfp8_quantize(_p(X), T, H, int(mode), _p(q), _p(sc))
     assert rc == 0
     return q, sc
+
+
+# ---- the post with an int8 layer output (x_scales) and the fused square sum ----
+
+def post_ex(R, prev_post, prev_comb, *, Y=None, Yq=None, x_scales=None):
+    """Step (1) with Y given as bf16 bits (Y) or as int8 codes Yq [T,H] with one fp32 scale per
+    token (x_scales [T]).  Returns (R' [T,4,H] bf16 bits, square sum of R' per token [T] fp64)."""
+    R = _c(R, np.uint16)
+    T, _, H = R.shape
+    pp = _c(prev_post, np.float32); pc = _c(prev_comb, np.float32)
+    Yb = None if Y is None else _c(Y, np.uint16)
+    Yi = None if Yq is None else _c(Yq, np.int8)
+    xs = None if x_scales is None else _c(x_scales, np.float32)
+    assert (Yb is None) != (Yi is None) and (Yi is None or xs is not None)
+    out = np.empty_like(R)
+    ss = np.empty(T)
+    rc = _load().oracle_post_ex(_p(R), _p(Yb), _p(Yi), _p(xs), _p(pp), _p(pc), T, H, _p(out), _p(ss))
+    assert rc == 0
+    return out, ss

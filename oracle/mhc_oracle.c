@@ -393,3 +393,46 @@ int oracle_mxfp8_quantize(const uint16_t *X /* [T][H] bf16 */, int64_t T, int64_
         }
     return 0;
 }
+
+/* ---- the mHC post with an int8 layer output and its fused square sum -----------------------
+ * [P1] "What this fixes": the int8 TileLang post kernels that consume the int8 all-reduced
+ * attention output together with its x_scales (VLLM_MHC_AR_INT8), and the post kernel's fused
+ * square sum (VLLM_MHC_POST_FUSE_SQRSUM).  The page gives no formula.  Readings (listed with the
+ * design notes): Y[t][h] = q[t][h] * x_scale[t] (one fp32 scale per token, exact in fp64 here),
+ * consumed in the post exactly as the bf16 Y is; the square sum of token t is
+ * sum over i, h of R'[i][h]^2 over the bf16-rounded R' (the value step (2) takes its mean of). */
+
+static void post_token_y(const uint16_t *R, const double *y, const float *post, const float *comb,
+                         int64_t H, uint16_t *Rout, double *sqrsum)
+{
+    double ss = 0.0;
+    for (int i = 0; i < HC; ++i) {
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = (double)post[i] * y[h];
+            for (int j = 0; j < HC; ++j)
+                acc += (double)comb[j * HC + i] * oracle_bf16_to_double(R[j * H + h]);
+            Rout[i * H + h] = oracle_double_to_bf16(acc);
+            double r = oracle_bf16_to_double(Rout[i * H + h]);
+            ss += r * r;
+        }
+    }
+    if (sqrsum) *sqrsum = ss;
+}
+
+/* Yq [T][H] int8 (or Y [T][H] bf16 when Yq is NULL), x_scales [T] -> Rout [T,4,H] bf16,
+ * sqrsum [T] (NULL to skip). */
+int oracle_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Yq, const float *x_scales,
+                   const float *prev_post, const float *prev_comb, int64_t T, int64_t H,
+                   uint16_t *Rout, double *sqrsum)
+{
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    if (!y) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h)
+            y[h] = Yq ? (double)Yq[t * H + h] * (double)x_scales[t] : oracle_bf16_to_double(Y[t * H + h]);
+        post_token_y(R + t * HC * H, y, prev_post + t * HC, prev_comb + t * HC * HC, H, Rout + t * HC * H,
+                     sqrsum ? sqrsum + t : NULL);
+    }
+    free(y);
+    return 0;
+}

@@ -522,3 +522,57 @@ def test_mxfp8_quantize_decodes_back_within_half_a_quantum(mode):
                     continue
                 be = max(math.floor(math.log2(sv)) if sv > 0 else -6, -6)
                 assert abs(dv - xv) <= 2.0 ** (E + be - 4) * (1 + 1e-12)   # half a quantum
+
+
+# ---------------------------------------------------------------- post with int8 Y and square sum
+
+def _post_inputs(T, H, seed):
+    rng = np.random.default_rng(seed)
+    R = bf(rng.standard_normal((T, 4, H)))
+    pp = (2.0 / (1.0 + np.exp(-rng.standard_normal((T, 4))))).astype(np.float32)
+    pc = rng.uniform(0.0, 0.5, (T, 4, 4)).astype(np.float32)
+    return rng, R, pp, pc
+
+
+def test_post_int8_reduces_to_the_bf16_post_when_q_times_scale_is_a_bf16_value():
+    # x_scale a power of two and |q| < 128: q * s has at most 7 significant bits, so it is a bf16
+    # value and the int8 post must equal the (pinned) bf16 post on Y = q * s bit for bit
+    T, H = 5, 96
+    rng, R, pp, pc = _post_inputs(T, H, 3)
+    q = rng.integers(-127, 128, (T, H)).astype(np.int8)
+    xs = (2.0 ** rng.integers(-12, 3, T)).astype(np.float32)
+    Y = bf(q.astype(np.float64) * xs[:, None])
+    assert np.array_equal(F(Y).astype(np.float64), q * xs[:, None].astype(np.float64))
+    got, _ = oracle.post_ex(R, pp, pc, Yq=q, x_scales=xs)
+    assert np.array_equal(got, oracle.post(R, Y, pp, pc))
+    got_b, _ = oracle.post_ex(R, pp, pc, Y=Y)
+    assert np.array_equal(got_b, got)
+
+
+def test_post_square_sum_closed_forms():
+    T, H = 4, 64
+    rng, R, pp, pc = _post_inputs(T, H, 4)
+    q = rng.integers(-127, 128, (T, H)).astype(np.int8)
+    xs = rng.uniform(0.001, 0.1, T).astype(np.float32)
+    # identity mix, zero post: R' = R, the square sum is that of R itself
+    eye = _identity_comb(T)
+    Rp, ss = oracle.post_ex(R, np.zeros((T, 4), np.float32), eye, Yq=q, x_scales=xs)
+    assert np.array_equal(Rp, R)
+    np.testing.assert_allclose(ss, (F(R).astype(np.float64) ** 2).sum(axis=(1, 2)), rtol=1e-13)
+    # zero mix, unit post: every stream is bf16(q * s); the sum is 4 * sum_h bf16(q * s)^2
+    Rp, ss = oracle.post_ex(R, np.ones((T, 4), np.float32), np.zeros((T, 4, 4), np.float32), Yq=q, x_scales=xs)
+    y = F(bf(q.astype(np.float64) * xs[:, None].astype(np.float64))).astype(np.float64)
+    for i in range(4):
+        assert np.array_equal(F(Rp[:, i, :]).astype(np.float64), y)
+    np.testing.assert_allclose(ss, 4 * (y ** 2).sum(axis=1), rtol=1e-13)
+
+
+def test_post_square_sum_matches_the_pre_step_rms():
+    # the pre step's r = 1/sqrt(ss/(4H) + eps) of the same R' (an independently pinned function)
+    T, H = 3, 128
+    rng, R, pp, pc = _post_inputs(T, H, 5)
+    Y = bf(rng.standard_normal((T, H)))
+    Rp, ss = oracle.post_ex(R, pp, pc, Y=Y)
+    phi, bias, ms, gamma = _zeros_weights(H)
+    out = oracle.pre(Rp, phi, bias, ms, gamma, **SC, debug=True)
+    np.testing.assert_allclose(out["r"], 1.0 / np.sqrt(ss / (4 * H) + SC["hc_norm_eps"]), rtol=1e-13)
