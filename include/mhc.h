@@ -208,6 +208,24 @@ MHC_API mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                     const float *prev_post_mix, const float *prev_comb_res_mix, int64_t T,
                     int64_t H, mhc_bf16 *residual_out, void *stream);
 
+/* Step (1) with the layer output as int8 codes and one fp32 scale per token (the consumer of
+ * an int8 all-reduce), plus the fused square sum: "[SM80] Backport mHC fused post + int8
+ * all-reduce; fixes #28, #29", "What this fixes" (VLLM_MHC_AR_INT8, VLLM_MHC_POST_FUSE_SQRSUM).
+ *   layer_out_q  [T,H] int8   codes q
+ *   x_scales     [T]   fp32   the layer output is Y[t][h] = q[t][h] * x_scales[t]
+ *   sqrsum_out   [T]   fp32   sum over i, h of R'[i][h]^2 of the bf16 residual_out (NULL: skip);
+ *                             fp32 accumulation in a fixed order (deterministic)
+ * Other arguments as in mhc_post (residual_out may equal residual).  Needs no workspace. */
+MHC_API mhc_status mhc_post_int8(const mhc_bf16 *residual, const int8_t *layer_out_q, const float *x_scales,
+                                 const float *prev_post_mix, const float *prev_comb_res_mix, int64_t T,
+                                 int64_t H, mhc_bf16 *residual_out, float *sqrsum_out, void *stream);
+
+/* mhc_post with the fused square sum (sqrsum_out [T] fp32, required; see mhc_post_int8).
+ * residual_out is bit-identical to mhc_post's. */
+MHC_API mhc_status mhc_post_sqrsum(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                                   const float *prev_post_mix, const float *prev_comb_res_mix, int64_t T,
+                                   int64_t H, mhc_bf16 *residual_out, float *sqrsum_out, void *stream);
+
 /* Steps (2)-(4) alone: the mHC pre, from streams that already went through the
  * post (`residual` here is R').  Same arguments and outputs as the fused call. */
 MHC_API mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const float *bias,

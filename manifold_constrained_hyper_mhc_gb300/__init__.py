@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
-    "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
+    "post_int8", "post_sqrsum", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
 ]
 MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
@@ -60,6 +60,10 @@ def lib():
             L.mhc_shifted_post_pre_mxfp8.restype = I
             L.mhc_mxfp8_scale_bytes.argtypes = [I64, I64]
             L.mhc_mxfp8_scale_bytes.restype = Z
+            L.mhc_post_int8.argtypes = [P, P, P, P, P, I64, I64, P, P, P]
+            L.mhc_post_int8.restype = I
+            L.mhc_post_sqrsum.argtypes = [P, P, P, P, I64, I64, P, P, P]
+            L.mhc_post_sqrsum.restype = I
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -218,6 +222,39 @@ def post(residual, layer_out, prev_post_mix, prev_comb_res_mix, *, out=None, str
                         T, H, _ptr(o), _stream(stream, residual.device))
     _check(rc, "mhc_post")
     return o
+
+
+def post_int8(residual, layer_out_q, x_scales, prev_post_mix, prev_comb_res_mix, *, sqrsum=True, out=None,
+              stream=None):
+    """mhc_post_int8: step (1) from an int8 layer output (codes [T,H] int8, x_scales [T] fp32).
+    Returns (residual_out [T,4,H] bf16, sqrsum [T] fp32 or None)."""
+    torch = _torch()
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H))
+    if layer_out_q.dtype != torch.int8 or tuple(layer_out_q.shape) != (T, H) or not layer_out_q.is_contiguous():
+        raise TypeError("layer_out_q must be a contiguous int8 [T, H] tensor")
+    _f32(x_scales, "x_scales", (T,))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    o = out if out is not None else torch.empty((T, 4, H), dtype=torch.bfloat16, device=residual.device)
+    ss = torch.empty(T, dtype=torch.float32, device=residual.device) if sqrsum else None
+    rc = lib().mhc_post_int8(_ptr(residual), _ptr(layer_out_q), _ptr(x_scales), _ptr(prev_post_mix),
+                             _ptr(prev_comb_res_mix), T, H, _ptr(o), _ptr(ss), _stream(stream, residual.device))
+    _check(rc, "mhc_post_int8")
+    return o, ss
+
+
+def post_sqrsum(residual, layer_out, prev_post_mix, prev_comb_res_mix, *, out=None, stream=None):
+    """mhc_post_sqrsum: mhc_post plus the square sum of R' per token.  Returns (residual_out, sqrsum)."""
+    torch = _torch()
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    o = out if out is not None else torch.empty((T, 4, H), dtype=torch.bfloat16, device=residual.device)
+    ss = torch.empty(max(T, 1), dtype=torch.float32, device=residual.device)[:T]
+    rc = lib().mhc_post_sqrsum(_ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix),
+                               T, H, _ptr(o), _ptr(ss), _stream(stream, residual.device))
+    _check(rc, "mhc_post_sqrsum")
+    return o, ss
 
 
 def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,

@@ -1,0 +1,88 @@
+// The mHC post (step (1)) with the layer output given as int8 codes and one fp32 scale per
+// token, and/or with the fused square sum of the updated streams: the post kernels of
+// "[SM80] Backport mHC fused post + int8 all-reduce; fixes #28, #29", "What this fixes"
+// (VLLM_MHC_AR_INT8 consumers, VLLM_MHC_POST_FUSE_SQRSUM).
+//
+// One CTA per token: it streams the token's 4 x H residual and its layer output once, writes
+// R' (the same fp32 expression and rounding as every other post), and, for the square sum,
+// adds R'^2 of the bf16-rounded values in a fixed order (per thread in vector order, then an
+// xor tree within each warp, then the warps in order), so the result is deterministic.
+#include <cstdint>
+
+#include "mhc_device.cuh"
+#include "mhc_kernels.h"
+
+namespace mhc {
+
+namespace {
+
+constexpr int kPT = 256;  // threads per CTA
+
+template <bool kInt8, bool kSq>
+__global__ void __launch_bounds__(kPT)
+post_ex_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, const int8_t *__restrict__ Yq,
+               const float *__restrict__ x_scales, const float *__restrict__ prev_post,
+               const float *__restrict__ prev_comb, int H, uint16_t *__restrict__ R_out,
+               float *__restrict__ sqrsum) {
+    __shared__ float sMix[20];  // comb [4][4], post [4]
+    __shared__ float sWarp[kPT / 32];
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (tid < 16) sMix[tid] = __ldg(prev_comb + t * 16 + tid);
+    else if (tid < 20) sMix[tid] = __ldg(prev_post + t * 4 + (tid - 16));
+    __syncthreads();
+    const float xs = kInt8 ? __ldg(x_scales + t) : 0.f;
+    const int nvec = H / kVec;
+    float ss = 0.f;
+    for (int v = tid; v < nvec; v += kPT) {
+        const int64_t base = t * kHC * (int64_t)H + (int64_t)v * kVec;
+        uint4 r[kHC];
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) r[j] = ld_stream(R + base + (int64_t)j * H);
+        float y[8];
+        if (kInt8) {
+            const uint2 q = __ldcs(reinterpret_cast<const uint2 *>(Yq + t * (int64_t)H + (int64_t)v * kVec));
+            const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = (float)(int8_t)(w[e >> 2] >> (8 * (e & 3))) * xs;
+        } else {
+            unpack8(ld_stream(Y + t * (int64_t)H + (int64_t)v * kVec), y);
+        }
+        uint4 o[kHC];
+        float rf[kHC][8];
+        post_vec8_yf(r, y, sMix, sMix + 16, o, rf);
+#pragma unroll
+        for (int i = 0; i < kHC; ++i) st_stream(R_out + base + (int64_t)i * H, o[i]);
+        if (kSq) {
+#pragma unroll
+            for (int i = 0; i < kHC; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(rf[i][e], rf[i][e], ss);
+        }
+    }
+    if (kSq) {
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) sWarp[tid >> 5] = ss;
+        __syncthreads();
+        if (tid == 0) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kPT / 32; ++w) a += sWarp[w];
+            sqrsum[t] = a;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Yq, const float *x_scales,
+                           const float *prev_post, const float *prev_comb, int64_t T, int H, uint16_t *R_out,
+                           float *sqrsum, cudaStream_t stream) {
+    const bool i8 = Yq != nullptr, sq = sqrsum != nullptr;
+    auto kern = i8 ? (sq ? post_ex_kernel<true, true> : post_ex_kernel<true, false>)
+                   : (sq ? post_ex_kernel<false, true> : post_ex_kernel<false, false>);
+    kern<<<(unsigned)T, kPT, 0, stream>>>(R, Y, Yq, x_scales, prev_post, prev_comb, H, R_out, sqrsum);
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <cstdint>
 #include <string>
 
 #include "mhc.h"
@@ -461,6 +462,64 @@ mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const f
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     g_launches = 1;
     return MHC_OK;
+}
+
+namespace {
+// Common body of mhc_post_int8 and mhc_post_sqrsum.
+mhc_status run_post_ex(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const int8_t *layer_out_q,
+                       const float *x_scales, const float *prev_post_mix, const float *prev_comb_res_mix,
+                       int64_t T, int64_t H, mhc_bf16 *residual_out, float *sqrsum_out, void *stream) {
+    mhc_status st;
+    g_launches = 0;
+    if ((st = check_sizes(T, H)) != MHC_OK) return st;
+    if (T > INT32_MAX) return fail(MHC_ERR_INVALID_ARG, "T too large");
+    if (T == 0) return MHC_OK;
+    const bool i8 = layer_out_q != nullptr;
+    if ((st = check_ptrs({{residual, "residual"}, {prev_post_mix, "prev_post_mix"},
+                          {prev_comb_res_mix, "prev_comb_res_mix"}, {residual_out, "residual_out"}})) != MHC_OK)
+        return st;
+    if (i8) {
+        if ((st = check_ptrs({{layer_out_q, "layer_out_q"}, {x_scales, "x_scales"}})) != MHC_OK) return st;
+    } else if ((st = check_ptrs({{layer_out, "layer_out"}})) != MHC_OK) {
+        return st;
+    }
+    if (sqrsum_out != nullptr && (st = check_ptrs({{sqrsum_out, "sqrsum_out"}})) != MHC_OK) return st;
+    const size_t tok = (size_t)T;
+    const Span o{residual_out, tok * 4 * H * 2}, oS{sqrsum_out, sqrsum_out ? tok * 4 : 0};
+    const Span ins[] = {{residual, tok * 4 * H * 2}, {layer_out, i8 ? 0 : tok * H * 2},
+                        {layer_out_q, i8 ? tok * H : 0}, {x_scales, i8 ? tok * 4 : 0},
+                        {prev_post_mix, tok * 16}, {prev_comb_res_mix, tok * 64}};
+    for (int i = 0; i < 6; ++i) {
+        if (i == 0 && residual_out == residual) continue;  // in-place residual update
+        if (overlap(o, ins[i])) return fail(MHC_ERR_INVALID_ARG, "residual_out overlaps an input");
+        if (overlap(oS, ins[i])) return fail(MHC_ERR_INVALID_ARG, "sqrsum_out overlaps an input");
+    }
+    if (overlap(o, oS)) return fail(MHC_ERR_INVALID_ARG, "sqrsum_out overlaps residual_out");
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
+    cudaError_t e = mhc::launch_post_ex(residual, i8 ? nullptr : layer_out, layer_out_q, x_scales, prev_post_mix,
+                                        prev_comb_res_mix, T, (int)H, residual_out, sqrsum_out,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches = 1;
+    return MHC_OK;
+}
+}  // namespace
+
+mhc_status mhc_post_int8(const mhc_bf16 *residual, const int8_t *layer_out_q, const float *x_scales,
+                         const float *prev_post_mix, const float *prev_comb_res_mix, int64_t T, int64_t H,
+                         mhc_bf16 *residual_out, float *sqrsum_out, void *stream) {
+    if (layer_out_q == nullptr && T > 0) return fail(MHC_ERR_INVALID_ARG, "layer_out_q is NULL");
+    return run_post_ex(residual, nullptr, layer_out_q, x_scales, prev_post_mix, prev_comb_res_mix, T, H,
+                       residual_out, sqrsum_out, stream);
+}
+
+mhc_status mhc_post_sqrsum(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+                           const float *prev_comb_res_mix, int64_t T, int64_t H, mhc_bf16 *residual_out,
+                           float *sqrsum_out, void *stream) {
+    if (sqrsum_out == nullptr && T > 0) return fail(MHC_ERR_INVALID_ARG, "sqrsum_out is NULL");
+    return run_post_ex(residual, layer_out, nullptr, nullptr, prev_post_mix, prev_comb_res_mix, T, H,
+                       residual_out, sqrsum_out, stream);
 }
 
 mhc_status mhc_set_schedule(int schedule) {

@@ -79,15 +79,14 @@ __device__ __forceinline__ void post_vec8(const uint4 (&r)[kHC], uint4 y, const 
     }
 }
 
-// Same arithmetic as post_vec8 on packed fp32 pairs (__fmul2_rn/__ffma2_rn):
-// each half of a packed operation is the same IEEE operation, so the results
-// are bit-identical to post_vec8; half the instructions.
-__device__ __forceinline__ void post_vec8_x2(const uint4 (&r)[kHC], uint4 y, const float *comb,
+// Same arithmetic as post_vec8 on packed fp32 pairs (__fmul2_rn/__ffma2_rn), with the
+// layer output given as 8 fp32 values: each half of a packed operation is the same IEEE
+// operation, so the results are bit-identical to post_vec8; half the instructions.
+__device__ __forceinline__ void post_vec8_yf(const uint4 (&r)[kHC], const float (&Y)[8], const float *comb,
                                              const float *post, uint4 (&out)[kHC], float (&rf)[kHC][8]) {
-    float R[kHC][8], Y[8];
+    float R[kHC][8];
 #pragma unroll
     for (int j = 0; j < kHC; ++j) unpack8(r[j], R[j]);
-    unpack8(y, Y);
 #pragma unroll
     for (int i = 0; i < kHC; ++i) {
         float acc[8];
@@ -106,6 +105,12 @@ __device__ __forceinline__ void post_vec8_x2(const uint4 (&r)[kHC], uint4 y, con
         out[i] = pack8_rn(acc);
         unpack8(out[i], rf[i]);
     }
+}
+__device__ __forceinline__ void post_vec8_x2(const uint4 (&r)[kHC], uint4 y, const float *comb,
+                                             const float *post, uint4 (&out)[kHC], float (&rf)[kHC][8]) {
+    float Y[8];
+    unpack8(y, Y);
+    post_vec8_yf(r, Y, comb, post, out, rf);
 }
 
 // ---- step (4): combine ------------------------------------------------------

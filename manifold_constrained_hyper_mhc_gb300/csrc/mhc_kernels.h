@@ -103,6 +103,12 @@ cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cu
 // (start) and after (stop) the launch of a call's main kernel.
 void mark_main_kernel(cudaStream_t stream, bool start);
 
+// The post with an int8 layer output (Yq, x_scales; Y unused) or a bf16 one (Y), and the
+// square sum of R' per token when sqrsum != nullptr (kernels_post.cu).  T < 2^31.
+cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Yq, const float *x_scales,
+                           const float *prev_post, const float *prev_comb, int64_t T, int H, uint16_t *R_out,
+                           float *sqrsum, cudaStream_t stream);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
