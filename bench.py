@@ -222,12 +222,35 @@ def run_ours(args, rank, world, lr, dist):
         out["layer_in_fp8"] = torch.empty((T, H), dtype=torch.uint8, device=dev)
         out["layer_in_scales"] = torch.empty(mhc.mxfp8_scale_bytes(T, H), dtype=torch.uint8, device=dev)
 
-    def call(R_, Y_, pp_, pc_):
-        if mx_mode is None:
-            mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=out, workspace=ws, stream=stream)
+    xsd = None
+    if args.op != "fused":
+        # the post variants: outputs R' (and the square sum); post_int8 takes the layer output as
+        # int8 codes with one scale per token (a symmetric per-token quantization of Y)
+        out = {"residual_out": out["residual_out"]}
+        if args.op != "post":
+            out["sqrsum"] = torch.empty(T, dtype=torch.float32, device=dev)
+        if args.op == "post_int8":
+            yf = synth.bf16_bits_to_f32(Y).astype(np.float64)
+            amax = np.abs(yf).max(axis=1)
+            xs = np.where(amax > 0, amax / 127.0, 1.0).astype(np.float32)
+            Y = np.clip(np.rint(yf / xs[:, None]), -127, 127).astype(np.int8)
+            Yd = torch.from_numpy(Y).to(dev)
+            xsd = torch.from_numpy(xs).to(dev)
+
+    def call(R_, Y_, pp_, pc_, st=stream):
+        if args.op == "post":
+            mhc.post(R_, Y_, pp_, pc_, out=out["residual_out"], stream=st)
+        elif args.op == "post_sqrsum":
+            mhc.lib().mhc_post_sqrsum(*[mhc._ptr(x) for x in (R_, Y_, pp_, pc_)], T, H,
+                                      mhc._ptr(out["residual_out"]), mhc._ptr(out["sqrsum"]), mhc._stream(st, dev))
+        elif args.op == "post_int8":
+            mhc.lib().mhc_post_int8(*[mhc._ptr(x) for x in (R_, Y_, xsd, pp_, pc_)], T, H,
+                                    mhc._ptr(out["residual_out"]), mhc._ptr(out["sqrsum"]), mhc._stream(st, dev))
+        elif mx_mode is None:
+            mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=out, workspace=ws, stream=st)
         else:
             mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode, out=out, workspace=ws,
-                                       stream=stream)
+                                       stream=st)
 
     def step():
         call(Rd, Yd, ppd, pcd)
@@ -246,10 +269,7 @@ def run_ours(args, rank, world, lr, dist):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gstream):
             for _ in range(args.graph):
-                mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=gstream) \
-                    if mx_mode is None else \
-                    mhc.shifted_post_pre_mxfp8(Rd, Yd, ppd, pcd, *wd, **sc, scale_mode=mx_mode, out=out,
-                                               workspace=ws, stream=gstream)
+                call(Rd, Yd, ppd, pcd, gstream)
         n_replay = max(1, args.steps // args.graph)
         args.steps = n_replay * args.graph
 
@@ -290,10 +310,7 @@ def run_ours(args, rank, world, lr, dist):
         with torch.cuda.graph(kg, stream=gstream2):
             for a_, b_ in kev:
                 mhc.set_main_kernel_events(a_, b_)
-                mhc.shifted_post_pre(Rd, Yd, ppd, pcd, *wd, **sc, out=out, workspace=ws, stream=gstream2) \
-                    if mx_mode is None else \
-                    mhc.shifted_post_pre_mxfp8(Rd, Yd, ppd, pcd, *wd, **sc, scale_mode=mx_mode, out=out,
-                                               workspace=ws, stream=gstream2)
+                call(Rd, Yd, ppd, pcd, gstream2)
             mhc.set_main_kernel_events(None, None)
         kg.replay()
     else:
@@ -313,7 +330,7 @@ def run_ours(args, rank, world, lr, dist):
     # e2e through the public API with host buffers: H2D of the step's inputs from
     # pinned memory, the call, D2H of its outputs, every step.
     hR = torch.from_numpy(R.view(np.int16)).pin_memory()
-    hY = torch.from_numpy(Y.view(np.int16)).pin_memory()
+    hY = torch.from_numpy(Y if Y.dtype == np.int8 else Y.view(np.int16)).pin_memory()
     hpp, hpc = torch.from_numpy(pp).pin_memory(), torch.from_numpy(pc).pin_memory()
     hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
     h2d = sum(t.numel() * t.element_size() for t in (hR, hY, hpp, hpc))
@@ -323,7 +340,7 @@ def run_ours(args, rank, world, lr, dist):
 
     def e2e_step():
         bufR.view(torch.int16).copy_(hR, non_blocking=True)
-        bufY.view(torch.int16).copy_(hY, non_blocking=True)
+        bufY.view(hY.dtype).copy_(hY, non_blocking=True)
         bufpp.copy_(hpp, non_blocking=True)
         bufpc.copy_(hpc, non_blocking=True)
         call(bufR, bufY, bufpp, bufpc)
@@ -349,16 +366,20 @@ def run_ours(args, rank, world, lr, dist):
     if rank != 0:
         return
     peak, peak_src = peaks()
-    abytes = algorithmic_bytes(T, H, mx_mode is not None)
+    abytes = algorithmic_bytes(T, H, mx_mode is not None) if args.op == "fused" else \
+        {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88)}[args.op]
     achieved = abytes / (kernel_ms / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
-        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
+        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op == "fused" else args.op
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H,
-                   "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)"),
+                   "op": {"fused": "mhc_shifted_post_pre", "post": "mhc_post", "post_sqrsum": "mhc_post_sqrsum",
+                          "post_int8": "mhc_post_int8"}[args.op],
+                   "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)")
+                         + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
                    "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -390,6 +411,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
+    ap.add_argument("--op", default="fused", choices=["fused", "post", "post_sqrsum", "post_int8"],
+                    help="the fused step (default) or one of the post-only entry points")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")
     ap.add_argument("--mxfp8", default="none", choices=["none", "floor", "ceil"],

@@ -81,7 +81,9 @@ cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Y
     const bool i8 = Yq != nullptr, sq = sqrsum != nullptr;
     auto kern = i8 ? (sq ? post_ex_kernel<true, true> : post_ex_kernel<true, false>)
                    : (sq ? post_ex_kernel<false, true> : post_ex_kernel<false, false>);
+    mark_main_kernel(stream, true);
     kern<<<(unsigned)T, kPT, 0, stream>>>(R, Y, Yq, x_scales, prev_post, prev_comb, H, R_out, sqrsum);
+    mark_main_kernel(stream, false);
     return cudaGetLastError();
 }
 

@@ -243,7 +243,9 @@ cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_
     int64_t blocks = (items + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)num_sms * 16;
     if (blocks > cap) blocks = cap;
+    mark_main_kernel(stream, true);
     post_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(R, Y, prev_post, prev_comb, T, H, R_out);
+    mark_main_kernel(stream, false);
     return cudaGetLastError();
 }
 
