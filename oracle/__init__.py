@@ -222,3 +222,17 @@ def post_ex(R, prev_post, prev_comb, *, Y=None, Yq=None, x_scales=None):
     rc = _load().oracle_post_ex(_p(R), _p(Yb), _p(Yi), _p(xs), _p(pp), _p(pc), T, H, _p(out), _p(ss))
     assert rc == 0
     return out, ss
+
+
+# ---- the first layer's pre: one (T, H) input broadcast to the 4 streams ----
+
+def pre_broadcast(x, phi, bias, mix_scales, gamma, **kw):
+    """Steps (2)-(4) on the residual made of 4 identical copies of x [T, H] (bf16 bits), the
+    first layer's case ("[DSv4.1] Integrate Mega-mHC from DeepGEMM": the (T, H) broadcast input
+    of mhc_pre_broadcast; the carried pre mix is None there).  Returns pre()'s dict plus
+    R = the broadcast residual [T, 4, H]."""
+    x = _c(x, np.uint16)
+    R = np.ascontiguousarray(np.repeat(x[:, None, :], 4, axis=1))
+    out = pre(R, phi, bias, mix_scales, gamma, **kw)
+    out["R"] = R
+    return out

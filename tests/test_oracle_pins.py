@@ -576,3 +576,31 @@ def test_post_square_sum_matches_the_pre_step_rms():
     phi, bias, ms, gamma = _zeros_weights(H)
     out = oracle.pre(Rp, phi, bias, ms, gamma, **SC, debug=True)
     np.testing.assert_allclose(out["r"], 1.0 / np.sqrt(ss / (4 * H) + SC["hc_norm_eps"]), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- first-layer broadcast pre
+
+def test_pre_broadcast_closed_forms():
+    """Four copies of x: the mean of the 4H squares is the mean over H, and the flattened
+    projection is x against the sum of phi's four row blocks, z = r * x @ (phi_0 + .. + phi_3).
+    X = (sum_i pre_i) x, so the layer input is x * s / sqrt(mean (s x)^2 + eps) * gamma."""
+    rng = np.random.default_rng(21)
+    T, H = 4, 96
+    x = bf(rng.standard_normal((T, H)))
+    phi = (rng.standard_normal((4 * H, 24)) * 0.05).astype(np.float32)
+    bias = (rng.standard_normal(24) * 0.1).astype(np.float32)
+    ms = np.array([0.7, 0.4, 0.3], np.float32)
+    gamma = bf(1.0 + 0.1 * rng.standard_normal(H))
+    out = oracle.pre_broadcast(x, phi, bias, ms, gamma, **SC, debug=True)
+    xd = F(x).astype(np.float64)
+    r = 1.0 / np.sqrt((xd ** 2).mean(axis=1) + SC["hc_norm_eps"])
+    np.testing.assert_allclose(out["r"], r, rtol=1e-13)
+    phisum = phi.astype(np.float64).reshape(4, H, 24).sum(axis=0)
+    np.testing.assert_allclose(out["z"], r[:, None] * (xd @ phisum), rtol=1e-10, atol=1e-13)
+    s = out["pre"].sum(axis=1)
+    X = s[:, None] * xd
+    want = X / np.sqrt((X ** 2).mean(axis=1, keepdims=True) + SC["rmsnorm_eps"]) * F(gamma).astype(np.float64)
+    got = F(out["X"]).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - 7)
+    assert np.all(np.abs(got - want) <= ulp)     # one bf16 rounding of the same value
+    assert np.array_equal(out["R"], np.repeat(x[:, None, :], 4, axis=1))
