@@ -223,7 +223,7 @@ def run_ours(args, rank, world, lr, dist):
         out["layer_in_scales"] = torch.empty(mhc.mxfp8_scale_bytes(T, H), dtype=torch.uint8, device=dev)
 
     xsd = None
-    if args.op != "fused":
+    if args.op not in ("fused", "pre_broadcast"):
         # the post variants: outputs R' (and the square sum); post_int8 takes the layer output as
         # int8 codes with one scale per token (a symmetric per-token quantization of Y)
         out = {"residual_out": out["residual_out"]}
@@ -237,8 +237,14 @@ def run_ours(args, rank, world, lr, dist):
             Yd = torch.from_numpy(Y).to(dev)
             xsd = torch.from_numpy(xs).to(dev)
 
+    if args.op == "pre_broadcast":
+        out = {"residual_out": out["residual_out"], "layer_in": out["layer_in"], "pre_mix": out["pre_mix"],
+               "post_mix": out["post_mix"], "comb_res_mix": out["comb_res_mix"]}
+
     def call(R_, Y_, pp_, pc_, st=stream):
-        if args.op == "post":
+        if args.op == "pre_broadcast":  # the first layer: Y plays the (T, H) input
+            mhc.pre_broadcast(Y_, *wd, **sc, out=out, workspace=ws, stream=st)
+        elif args.op == "post":
             mhc.post(R_, Y_, pp_, pc_, out=out["residual_out"], stream=st)
         elif args.op == "post_sqrsum":
             mhc.lib().mhc_post_sqrsum(*[mhc._ptr(x) for x in (R_, Y_, pp_, pc_)], T, H,
@@ -367,7 +373,8 @@ def run_ours(args, rank, world, lr, dist):
         return
     peak, peak_src = peaks()
     abytes = algorithmic_bytes(T, H, mx_mode is not None) if args.op == "fused" else \
-        {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88)}[args.op]
+        {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88),
+         "pre_broadcast": T * (12 * H + 96) + 384 * H + 2 * H + 108}[args.op]
     achieved = abytes / (kernel_ms / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
         {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op == "fused" else args.op
@@ -377,7 +384,7 @@ def run_ours(args, rank, world, lr, dist):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H,
                    "op": {"fused": "mhc_shifted_post_pre", "post": "mhc_post", "post_sqrsum": "mhc_post_sqrsum",
-                          "post_int8": "mhc_post_int8"}[args.op],
+                          "post_int8": "mhc_post_int8", "pre_broadcast": "mhc_pre_broadcast"}[args.op],
                    "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)")
                          + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
@@ -411,7 +418,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
-    ap.add_argument("--op", default="fused", choices=["fused", "post", "post_sqrsum", "post_int8"],
+    ap.add_argument("--op", default="fused", choices=["fused", "post", "post_sqrsum", "post_int8", "pre_broadcast"],
                     help="the fused step (default) or one of the post-only entry points")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")

@@ -235,6 +235,20 @@ MHC_API mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const flo
                    float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
                    void *workspace, size_t workspace_bytes, void *stream);
 
+/* The first layer's pre: the residual does not exist yet and the layer's (T, H) input x is
+ * broadcast to the four streams ("[DSv4.1] Integrate Mega-mHC from DeepGEMM", "Paths on current
+ * main that still call DeepGEMM on SM12x" item 1, mhc_pre_broadcast; the None pre mix of "Nit"
+ * 6 only occurs here).  Writes residual_out [T,4,H] = four copies of x (what the next layer's
+ * post reads), then computes steps (2)-(4) on it exactly as mhc_pre does (same outputs,
+ * bit-identical to mhc_pre on that residual).  x must not overlap any output. */
+MHC_API mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *bias,
+                                     const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T,
+                                     int64_t H, float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                                     float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+                                     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                                     float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
 /* Forces a schedule for every following call of this process (a test hook; the
  * default is MHC_SCHEDULE_AUTO).  Returns MHC_ERR_INVALID_ARG for an unknown value. */
 MHC_API mhc_status mhc_set_schedule(int schedule);

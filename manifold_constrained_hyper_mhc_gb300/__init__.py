@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
-    "post_int8", "post_sqrsum", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
+    "post_int8", "post_sqrsum", "pre_broadcast", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
 ]
 MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
@@ -64,6 +64,8 @@ def lib():
             L.mhc_post_int8.restype = I
             L.mhc_post_sqrsum.argtypes = [P, P, P, P, I64, I64, P, P, P]
             L.mhc_post_sqrsum.restype = I
+            L.mhc_pre_broadcast.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, P, Z, P]
+            L.mhc_pre_broadcast.restype = I
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -274,6 +276,26 @@ def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm
                        _ptr(o["comb_res_mix"]), _ptr(ws), ws.numel() * ws.element_size(),
                        _stream(stream, dev))
     _check(rc, "mhc_pre")
+    return o
+
+
+def pre_broadcast(x, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,
+                  sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None):
+    """mhc_pre_broadcast: the first layer's pre from the (T, H) input x.  Returns the dict of
+    pre() plus residual_out [T,4,H] (four copies of x)."""
+    T, H = x.shape
+    _bf16(x, "x", (T, H))
+    _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
+    _bf16(rmsnorm_weight, "rmsnorm_weight", (H,))
+    dev = x.device
+    o = _outputs(T, H, dev, out, True)
+    ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    rc = lib().mhc_pre_broadcast(_ptr(x), _ptr(phi), _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H,
+                                 hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, int(sinkhorn_iters),
+                                 _ptr(o["residual_out"]), _ptr(o["layer_in"]), _ptr(o["pre_mix"]),
+                                 _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream, dev))
+    _check(rc, "mhc_pre_broadcast")
     return o
 
 

@@ -73,7 +73,29 @@ post_ex_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, c
     }
 }
 
+// The first layer's residual: four copies of the (T, H) input, R[t][j] = x[t] (plain stores:
+// a following pre reads them back, from L2 when they fit).
+__global__ void __launch_bounds__(kPT)
+broadcast4_kernel(const uint16_t *__restrict__ x, int64_t n_vec, int nvec_row, int H, uint16_t *__restrict__ R) {
+    for (int64_t i = (int64_t)blockIdx.x * kPT + threadIdx.x; i < n_vec; i += (int64_t)gridDim.x * kPT) {
+        const int64_t t = i / nvec_row;
+        const int v = (int)(i % nvec_row);
+        const uint4 a = ld_stream(x + t * (int64_t)H + (int64_t)v * kVec);
+        uint16_t *dst = R + t * kHC * (int64_t)H + (int64_t)v * kVec;
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) *reinterpret_cast<uint4 *>(dst + (int64_t)j * H) = a;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_broadcast4(const uint16_t *x, int64_t T, int H, uint16_t *R_out, int num_sms, cudaStream_t stream) {
+    const int nvec = H / kVec;
+    const int64_t n = T * nvec;
+    const int64_t want = (n + kPT - 1) / kPT, cap = (int64_t)num_sms * 8;
+    broadcast4_kernel<<<(unsigned)(want < cap ? want : cap), kPT, 0, stream>>>(x, n, nvec, H, R_out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Yq, const float *x_scales,
                            const float *prev_post, const float *prev_comb, int64_t T, int H, uint16_t *R_out,

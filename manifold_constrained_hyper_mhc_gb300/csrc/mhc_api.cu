@@ -438,6 +438,53 @@ mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const float *bias
                         workspace_bytes, stream, false);
 }
 
+mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *bias, const float *mix_scales,
+                             const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps,
+                             float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters,
+                             mhc_bf16 *residual_out, mhc_bf16 *layer_in_out, float *pre_mix_out,
+                             float *post_mix_out, float *comb_res_mix_out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    mhc_status st;
+    g_launches = 0;
+    if ((st = check_sizes(T, H)) != MHC_OK) return st;
+    if ((st = check_scalars(hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters)) != MHC_OK)
+        return st;
+    if (T == 0) return MHC_OK;
+    if ((st = check_ptrs({{x, "x"}, {residual_out, "residual_out"}})) != MHC_OK) return st;
+    const size_t tok = (size_t)T;
+    const Span sx{x, tok * H * 2};
+    const Span outs[] = {{residual_out, tok * 4 * H * 2}, {layer_in_out, tok * H * 2}, {pre_mix_out, tok * 16},
+                         {post_mix_out, tok * 16}, {comb_res_mix_out, tok * 64},
+                         {workspace, workspace_bytes < workspace_bytes_for(T, H) ? workspace_bytes
+                                                                                : workspace_bytes_for(T, H)}};
+    const Span ins[] = {sx, {phi, (size_t)H * 4 * 24 * 4}, {bias, 96}, {mix_scales, 12}, {rmsnorm_weight, (size_t)H * 2}};
+    for (int a = 0; a < 6; ++a) {
+        for (const Span &i : ins)
+            if (overlap(outs[a], i)) return fail(MHC_ERR_INVALID_ARG, "an output overlaps an input");
+        for (int b = a + 1; b < 6; ++b)
+            if (overlap(outs[a], outs[b])) return fail(MHC_ERR_INVALID_ARG, "two outputs overlap");
+    }
+    // the pre's own checks (pointers, workspace, overlaps of its inputs and outputs) run before
+    // anything is launched: validate by a dry run first
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
+    if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
+    if (workspace_bytes < workspace_bytes_for(T, H))
+        return fail(MHC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, workspace_bytes_for(T, H));
+    if ((st = check_ptrs({{phi, "phi"}, {bias, "bias"}, {mix_scales, "mix_scales"}, {rmsnorm_weight, "rmsnorm_weight"},
+                          {layer_in_out, "layer_in_out"}, {pre_mix_out, "pre_mix_out"}, {post_mix_out, "post_mix_out"},
+                          {comb_res_mix_out, "comb_res_mix_out"}})) != MHC_OK)
+        return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mhc::launch_broadcast4(x, T, (int)H, residual_out, dev.sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    st = run_post_pre(residual_out, nullptr, nullptr, nullptr, phi, bias, mix_scales, rmsnorm_weight, T, H,
+                      hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters, nullptr, layer_in_out,
+                      pre_mix_out, post_mix_out, comb_res_mix_out, workspace, workspace_bytes, stream, false);
+    if (st == MHC_OK) g_launches += 1;
+    return st;
+}
+
 mhc_status mhc_post(const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
                     const float *prev_comb_res_mix, int64_t T, int64_t H, mhc_bf16 *residual_out,
                     void *stream) {

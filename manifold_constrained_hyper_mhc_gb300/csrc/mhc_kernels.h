@@ -109,6 +109,9 @@ cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Y
                            const float *prev_post, const float *prev_comb, int64_t T, int H, uint16_t *R_out,
                            float *sqrsum, cudaStream_t stream);
 
+// R_out[t][j] = x[t] for the four streams (kernels_post.cu).
+cudaError_t launch_broadcast4(const uint16_t *x, int64_t T, int H, uint16_t *R_out, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
