@@ -241,8 +241,38 @@ def run_ours(args, rank, world, lr, dist):
         out = {"residual_out": out["residual_out"], "layer_in": out["layer_in"], "pre_mix": out["pre_mix"],
                "post_mix": out["post_mix"], "comb_res_mix": out["comb_res_mix"]}
 
+    if args.op == "split":
+        # two workspaces and event pairs: call i waits on the join of call i-2, so the side
+        # kernel of call i (post and residual mixes) overlaps the main kernel of call i+1
+        side = torch.cuda.Stream(dev)
+        wss = [ws, mhc.new_workspace(T, H, dev)]
+        sevs = []
+        ncall = [0]
+
+    def fresh_split_events():
+        """New event pairs (an event recorded inside a stream capture cannot be waited on
+        outside it, so each capture and the eager phase get their own)."""
+        if args.op != "split":
+            return
+        torch.cuda.synchronize(dev)
+        sevs[:] = [(torch.cuda.Event(), torch.cuda.Event()) for _ in range(2)]
+        for f_, j_ in sevs:
+            f_.record(stream)
+            j_.record(stream)
+        torch.cuda.synchronize(dev)
+        ncall[0] = 0
+    fresh_split_events()
+
     def call(R_, Y_, pp_, pc_, st=stream):
-        if args.op == "pre_broadcast":  # the first layer: Y plays the (T, H) input
+        if args.op == "split":
+            i = ncall[0]
+            ncall[0] += 1
+            f_, j_ = sevs[i % 2]
+            if i >= 2:
+                st.wait_event(j_)
+            mhc.shifted_post_pre_split(R_, Y_, pp_, pc_, *wd, **sc, side_stream=side, fork_event=f_, join_event=j_,
+                                       out=out, workspace=wss[i % 2], stream=st)
+        elif args.op == "pre_broadcast":  # the first layer: Y plays the (T, H) input  # the first layer: Y plays the (T, H) input
             mhc.pre_broadcast(Y_, *wd, **sc, out=out, workspace=ws, stream=st)
         elif args.op == "post":
             mhc.post(R_, Y_, pp_, pc_, out=out["residual_out"], stream=st)
@@ -273,9 +303,13 @@ def run_ours(args, rank, world, lr, dist):
         gstream = torch.cuda.Stream(dev)
         gstream.wait_stream(stream)
         g = torch.cuda.CUDAGraph()
+        fresh_split_events()
         with torch.cuda.graph(g, stream=gstream):
             for _ in range(args.graph):
                 call(Rd, Yd, ppd, pcd, gstream)
+            if args.op == "split":  # join the side stream back
+                for f_, j_ in sevs:
+                    gstream.wait_event(j_)
         n_replay = max(1, args.steps // args.graph)
         args.steps = n_replay * args.graph
 
@@ -313,11 +347,15 @@ def run_ours(args, rank, world, lr, dist):
         kg = torch.cuda.CUDAGraph()
         gstream2 = torch.cuda.Stream(dev)
         gstream2.wait_stream(stream)
+        fresh_split_events()
         with torch.cuda.graph(kg, stream=gstream2):
             for a_, b_ in kev:
                 mhc.set_main_kernel_events(a_, b_)
                 call(Rd, Yd, ppd, pcd, gstream2)
             mhc.set_main_kernel_events(None, None)
+            if args.op == "split":
+                for f_, j_ in sevs:
+                    gstream2.wait_event(j_)
         kg.replay()
     else:
         for a_, b_ in kev:
@@ -333,6 +371,7 @@ def run_ours(args, rank, world, lr, dist):
     ms_step = el_ms / args.steps
     value = world * T / (ms_step / 1e3)
 
+    fresh_split_events()
     # e2e through the public API with host buffers: H2D of the step's inputs from
     # pinned memory, the call, D2H of its outputs, every step.
     hR = torch.from_numpy(R.view(np.int16)).pin_memory()
@@ -372,19 +411,20 @@ def run_ours(args, rank, world, lr, dist):
     if rank != 0:
         return
     peak, peak_src = peaks()
-    abytes = algorithmic_bytes(T, H, mx_mode is not None) if args.op == "fused" else \
+    abytes = algorithmic_bytes(T, H, mx_mode is not None) if args.op in ("fused", "split") else \
         {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88),
          "pre_broadcast": T * (12 * H + 96) + 384 * H + 2 * H + 108}[args.op]
     achieved = abytes / (kernel_ms / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
-        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op == "fused" else args.op
+        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op in ("fused", "split") else args.op
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H,
                    "op": {"fused": "mhc_shifted_post_pre", "post": "mhc_post", "post_sqrsum": "mhc_post_sqrsum",
-                          "post_int8": "mhc_post_int8", "pre_broadcast": "mhc_pre_broadcast"}[args.op],
+                          "post_int8": "mhc_post_int8", "pre_broadcast": "mhc_pre_broadcast",
+                          "split": "mhc_shifted_post_pre_split (mixes on a side stream)"}[args.op],
                    "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)")
                          + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
@@ -418,7 +458,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
-    ap.add_argument("--op", default="fused", choices=["fused", "post", "post_sqrsum", "post_int8", "pre_broadcast"],
+    ap.add_argument("--op", default="fused",
+                    choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre_broadcast"],
                     help="the fused step (default) or one of the post-only entry points")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")

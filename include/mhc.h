@@ -137,6 +137,31 @@ MHC_API mhc_status mhc_shifted_post_pre(
     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
     void *workspace, size_t workspace_bytes, void *stream);
 
+/* The fused step with its off-critical-path part on a second stream ("[DSV4.1] Four BS=1
+ * critical-path fixes for DSpark decode", "Measured and deliberately left out": the split
+ * path keeps the mHC statistics and Sinkhorn off the main stream).  Arguments and outputs as in
+ * mhc_shifted_post_pre, plus:
+ *   side_stream   a cudaStream_t other than `stream`
+ *   fork_event,   cudaEvent_t handles owned by the caller (cudaEventDisableTiming is fine)
+ *   join_event
+ * On `stream`: residual_out, layer_in_out and pre_mix_out (everything the next sublayer needs).
+ * fork_event is recorded on `stream` once the per-CTA records are in the workspace; side_stream
+ * waits on it, computes post_mix_out and comb_res_mix_out (the Sinkhorn) from those records,
+ * and join_event is recorded on side_stream after them.  The caller makes whatever reads the
+ * post or residual mix, and the next call that uses this workspace, wait on join_event (e.g.
+ * cudaStreamWaitEvent(stream, join_event) before the next layer's call; under stream capture
+ * this also joins side_stream back).  Results are bit-identical to mhc_shifted_post_pre on the
+ * same schedule.  Only the small schedule (AUTO for T <= 32) has a side part; on the others
+ * every output is produced on `stream` and the events are still recorded and waited on. */
+MHC_API mhc_status mhc_shifted_post_pre_split(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,
+    const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps,
+    float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+    void *workspace, size_t workspace_bytes, void *stream, void *side_stream, void *fork_event,
+    void *join_event);
+
 /* MXFP8 block-scale rules for the quantized layer input (the pages name MXFP8 and the
  * UE8M0 scale byte but give no formula; both rules are offered). */
 typedef enum mhc_mx_scale_mode {

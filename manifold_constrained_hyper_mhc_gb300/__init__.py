@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
-    "post_int8", "post_sqrsum", "pre_broadcast", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
+    "post_int8", "post_sqrsum", "pre_broadcast", "shifted_post_pre_split", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
 ]
 MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
@@ -66,6 +66,9 @@ def lib():
             L.mhc_post_sqrsum.restype = I
             L.mhc_pre_broadcast.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, P, Z, P]
             L.mhc_pre_broadcast.restype = I
+            L.mhc_shifted_post_pre_split.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
+                                                     P, P, P, P, P, P, Z, P, P, P, P]
+            L.mhc_shifted_post_pre_split.restype = I
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -174,6 +177,32 @@ def shifted_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi,
         _ptr(o["pre_mix"]), _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream, dev))
     _check(rc, "mhc_shifted_post_pre")
+    return o
+
+
+def shifted_post_pre_split(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                           rmsnorm_weight, *, side_stream, fork_event, join_event, hc_norm_eps, rmsnorm_eps,
+                           hc_post_scale, sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None):
+    """mhc_shifted_post_pre_split: the fused step with the post and residual mixes computed on
+    side_stream (torch.cuda.Stream); fork_event / join_event are torch.cuda.Event objects (already
+    created, e.g. recorded once).  Wait on join_event before reading post_mix / comb_res_mix or
+    reusing the workspace."""
+    T, _, H = residual.shape
+    _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
+    _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
+    _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
+    _bf16(rmsnorm_weight, "rmsnorm_weight", (H,))
+    dev = residual.device
+    o = _outputs(T, H, dev, out, True)
+    ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    rc = lib().mhc_shifted_post_pre_split(
+        _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
+        _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
+        hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
+        _ptr(o["pre_mix"]), _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream, dev), ctypes.c_void_p(side_stream.cuda_stream),
+        ctypes.c_void_p(fork_event.cuda_event), ctypes.c_void_p(join_event.cuda_event))
+    _check(rc, "mhc_shifted_post_pre_split")
     return o
 
 

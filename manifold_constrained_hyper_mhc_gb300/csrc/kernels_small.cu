@@ -168,7 +168,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
              const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int T, int H,
              int Hs, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
              float *__restrict__ post_out, float *__restrict__ res_out, float *__restrict__ part,
-             unsigned int *__restrict__ ctrl, MxOut mx) {
+             unsigned int *__restrict__ ctrl, MxOut mx, int split) {
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, nc = gridDim.x;
@@ -372,7 +372,8 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         return;
     }
 
-    const bool owner_cta = c < T;
+    // split: no owner warps; the post and residual mixes are left to small_tail_kernel
+    const bool owner_cta = !split && c < T;
     if (owner_cta && warp == 0) {
         // ---- token c (and c + nc, ...): logits 4..23 summed over the CTAs; pre logits and r from
         // the workers' sums; heads and the Sinkhorn mix.
@@ -448,6 +449,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         *reinterpret_cast<float4 *>(sSt + t * 8) = make_float4(pre[0], pre[1], pre[2], pre[3]);
         sSt[t * 8 + 4] = rstd;
         sSt[t * 8 + 5] = r;
+        if (split && c == 0) *reinterpret_cast<float4 *>(pre_out + (size_t)t * 4) = make_float4(pre[0], pre[1], pre[2], pre[3]);
     }
     wsync();
     if (owner_cta) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums and stats -> owner warp
@@ -475,6 +477,31 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
                          mx.scale + mx_scale_offset(t, (h0 + v * kVec) / 32, H));
     }
     if (dead && wt == 0) atomicOr(ctrl, 1u);
+}
+
+// The post and residual mixes of token blockIdx.x from the records a split small_kernel left
+// in the workspace: the same sums in the same order as the kernel's owner warp (so the
+// same bits), then the heads and the Sinkhorn.  One warp per token.
+__global__ void __launch_bounds__(32)
+small_tail_kernel(const float *__restrict__ part, int T, int nc, int H, const float *__restrict__ bias,
+                  const float *__restrict__ mix_scales, Scalars sc, float *__restrict__ post_out,
+                  float *__restrict__ res_out) {
+    __shared__ __align__(16) float sv[28];  // head slots 0..7, then logits 4..23
+    const int t = blockIdx.x, lane = threadIdx.x;
+    const float *heads = part + (size_t)t * nc * kHead;
+    const float *tails = part + (size_t)T * nc * kHead + (size_t)t * nc * kTail;
+    const float4 h4 = warp_cta_sum16(heads, kHead, nc, 2);        // pre logits, Gram diagonal
+    const float4 ta = warp_cta_sum16(tails, kTail, nc, 4);        // logits 4..19
+    const float4 tb = warp_cta_sum16(tails + 16, kTail, nc, 1);   // logits 20..23
+    if (lane < 2) *reinterpret_cast<float4 *>(sv + 4 * lane) = h4;
+    if (lane < 4) *reinterpret_cast<float4 *>(sv + 8 + 4 * lane) = ta;
+    if (lane == 0) *reinterpret_cast<float4 *>(sv + 24) = tb;
+    __syncwarp();
+    const float r = hc_rsqrt((sv[4] + sv[5]) + (sv[6] + sv[7]), H, sc.hc_norm_eps);
+    const float z = r * (lane < 4 ? sv[lane] : (lane < kNumMix ? sv[lane + 4] : 0.f));
+    const float v = heads_and_sinkhorn(z, bias, mix_scales, sc);
+    if (lane >= 4 && lane < 8) post_out[(size_t)t * 4 + lane - 4] = v;
+    else if (lane >= 8 && lane < kNumMix) res_out[(size_t)t * 16 + lane - 8] = v;
 }
 
 }  // namespace
@@ -525,9 +552,16 @@ cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cu
     mark_main_kernel(stream, true);
     e = cudaLaunchKernelEx(&cfg, kern, a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.bias, a.mix_scales, a.gamma,
                            a.s, (int)a.T, a.H, Hs, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, a.part,
-                           ctrl, a.mx);
+                           ctrl, a.mx, a.side != nullptr ? 1 : 0);
     mark_main_kernel(stream, false);
-    return e;
+    if (e != cudaSuccess || a.side == nullptr) return e;
+    // split: the mixes on the side stream, after the records are in
+    if ((e = cudaEventRecord(a.side->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(a.side->stream, a.side->fork, 0)) != cudaSuccess) return e;
+    small_tail_kernel<<<(unsigned)a.T, 32, 0, a.side->stream>>>(a.part, (int)a.T, n, a.H, a.bias, a.mix_scales, a.s,
+                                                                a.post_out, a.res_out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaEventRecord(a.side->join, a.side->stream);
 }
 
 }  // namespace mhc

@@ -163,7 +163,8 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                         int sinkhorn_iters, mhc_bf16 *residual_out, mhc_bf16 *layer_in_out,
                         float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
                         void *workspace, size_t workspace_bytes, void *stream, bool fused,
-                        uint8_t *mx_q = nullptr, uint8_t *mx_scale = nullptr, int mx_mode = 0) {
+                        uint8_t *mx_q = nullptr, uint8_t *mx_scale = nullptr, int mx_mode = 0,
+                        const mhc::SideStream *side = nullptr) {
     mhc_status st;
     g_launches = 0;
     const bool mx = mx_q != nullptr || mx_scale != nullptr;
@@ -331,8 +332,10 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.res_out = comb_res_mix_out;
             a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
             a.mx = mxo;
+            a.side = side;
             e = mhc::launch_small(a, static_cast<unsigned int *>(workspace), dev.sms, cs);
-            g_launches = 1;
+            g_launches = side != nullptr ? 2 : 1;
+            side = nullptr;  // done: the tail kernel ran on the side stream
             break;
         }
         case MHC_SCHEDULE_CLUSTER16: {
@@ -353,6 +356,13 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
         }
         default:
             return fail(MHC_ERR_UNSUPPORTED, "schedule %d is not available", sched);
+    }
+    if (e == cudaSuccess && side != nullptr) {
+        // a split call on a schedule without a side part: the mixes are complete on the main
+        // stream; the side stream still gets the fork and the join, so the contract holds
+        e = cudaEventRecord(side->fork, cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
     }
     if (e != cudaSuccess) {
         g_launches = 0;
@@ -401,6 +411,31 @@ mhc_status mhc_shifted_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_
                         rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
                         sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
                         comb_res_mix_out, workspace, workspace_bytes, stream, true);
+}
+
+mhc_status mhc_shifted_post_pre_split(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                                      const float *prev_post_mix, const float *prev_comb_res_mix,
+                                      const float *phi, const float *bias, const float *mix_scales,
+                                      const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
+                                      float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                                      float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+                                      mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                                      float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                      void *stream, void *side_stream, void *fork_event, void *join_event) {
+    if (fork_event == nullptr || join_event == nullptr) {
+        g_launches = 0;
+        return fail(MHC_ERR_INVALID_ARG, "fork_event and join_event must be events");
+    }
+    if (side_stream == stream) {
+        g_launches = 0;
+        return fail(MHC_ERR_INVALID_ARG, "side_stream must differ from stream");
+    }
+    const mhc::SideStream side{static_cast<cudaStream_t>(side_stream), static_cast<cudaEvent_t>(fork_event),
+                               static_cast<cudaEvent_t>(join_event)};
+    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                        comb_res_mix_out, workspace, workspace_bytes, stream, true, nullptr, nullptr, 0, &side);
 }
 
 size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H) {

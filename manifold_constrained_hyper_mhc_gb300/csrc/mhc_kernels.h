@@ -18,6 +18,14 @@ constexpr int kPartStride = 32;  // floats per (token, chunk) record: z[24], squ
 // (device status word, barrier counters).
 constexpr size_t kControlBytes = 256;
 
+// A second stream for the off-critical-path part of a split call: `fork` is recorded on the
+// main stream once the records are in, the side stream waits on it, and `join` is recorded on
+// the side stream after its work.
+struct SideStream {
+    cudaStream_t stream;
+    cudaEvent_t fork, join;
+};
+
 struct SplitArgs {
     const uint16_t *R;  // residual (fused) or already post-updated residual (pre only)
     const uint16_t *Y;
@@ -31,6 +39,7 @@ struct SplitArgs {
     float *pre_out, *post_out, *res_out;
     float *part;  // workspace: [T][ceil(H/256)][32] floats
     MxOut mx;     // MXFP8 layer input (mx.q == nullptr: none)
+    const SideStream *side;  // small schedule only: post and residual mixes on a side stream (nullptr: no)
 };
 
 inline size_t split_workspace_bytes(int64_t T, int64_t H) {
