@@ -91,6 +91,9 @@ struct FusedSmem {
 // (stream i, hidden h) as k_local = i*Hs + (h - c*Hs); zero where h >= H.
 __global__ void __launch_bounds__(256)
 pack_phi_kernel(const float *__restrict__ phi, int H, int C, int Hs, uint4 *__restrict__ out) {
+    // a kernel launched after this one with programmatic stream serialization may start now;
+    // it waits for this grid's results before reading them
+    asm volatile("griddepcontrol.launch_dependents;");
     const int S = kHC * Hs / 16;
     const int64_t total = (int64_t)C * S * 3 * 32;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

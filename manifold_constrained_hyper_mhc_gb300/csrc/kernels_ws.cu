@@ -259,6 +259,9 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             if (((p2 + kWP2) & 3) == (warp & 3)) col0 += 64 * nblk(p2);
         tq = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col0;
         const uint4 *pack = phi_pack + (size_t)c * (kHC * Hs / 16) * 96;
+        // the kernel may start while the packing launch before it still runs (programmatic
+        // dependent launch): wait for its results here, the only place that reads them
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int i = 0; i < nblk(p); ++i) {
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
@@ -823,11 +826,15 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static int max_clusters[64][4];
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // overlap the start (shared-memory and barrier setup, the first tile loads) with the
+    // packing launch; the projection warps wait for the packed phi (griddepcontrol.wait)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kNT);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -852,6 +859,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         }
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
+    cfg.numAttrs = 2;
     mark_main_kernel(stream, true);
     e = cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
                            a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);
