@@ -396,9 +396,10 @@ def run_ours(args, rank, world, lr, dist):
         b_["ev_free"].record(s_out)
     torch.cuda.synchronize(dev)
 
-    def e2e_step(i):
+    def e2e_step(i, capturing=False):
         b_ = sets[i % 2]
-        s_in.wait_event(b_["ev_free"])            # step i-2 is done with this set
+        if not (capturing and i < 2):  # inside a capture, only events recorded in it can be waited on
+            s_in.wait_event(b_["ev_free"])        # step i-2 is done with this set
         with torch.cuda.stream(s_in):
             b_["R"].view(torch.int16).copy_(hR, non_blocking=True)
             b_["Y"].view(hY.dtype).copy_(hY, non_blocking=True)
@@ -419,12 +420,46 @@ def run_ours(args, rank, world, lr, dist):
         e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(s_out)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if args.graph > 0:
+        # launch-bound sizes: the same pipelined steps captured into one CUDA graph (forked onto
+        # the copy streams and joined back inside the capture), replayed
+        fresh_split_events()
+        cs0 = torch.cuda.Stream(dev)
+        cs0.wait_stream(stream)
+        eg = torch.cuda.CUDAGraph()
+        stream_saved = stream
+        with torch.cuda.graph(eg, stream=cs0):
+            stream = cs0
+            fork = torch.cuda.Event()
+            fork.record(cs0)
+            s_in.wait_event(fork)
+            s_out.wait_event(fork)
+            for i in range(args.graph):
+                e2e_step(i, capturing=True)
+            for st_ in (s_in, s_out):
+                jn = torch.cuda.Event()
+                jn.record(st_)
+                cs0.wait_event(jn)
+            if args.op == "split":  # the side stream of the last calls
+                for f_, j_ in sevs:
+                    cs0.wait_event(j_)
+        stream = stream_saved
+        eg.replay()
+        torch.cuda.synchronize(dev)
+        n_rep = max(1, e2e_steps // args.graph)
+        e0.record(stream)
+        for _ in range(n_rep):
+            eg.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / (n_rep * args.graph)
+    else:
+        e0.record(s_in)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if dist is not None:
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
