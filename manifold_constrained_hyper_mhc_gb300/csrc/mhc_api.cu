@@ -499,10 +499,7 @@ mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *b
         for (int b = a + 1; b < 6; ++b)
             if (overlap(outs[a], outs[b])) return fail(MHC_ERR_INVALID_ARG, "two outputs overlap");
     }
-    // the pre's own checks (pointers, workspace, overlaps of its inputs and outputs) run before
-    // anything is launched: validate by a dry run first
-    Device dev;
-    if ((st = current_device(dev)) != MHC_OK) return st;
+    // the pre's own checks (pointers, workspace) also run here, before anything is launched
     if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
     if (workspace_bytes < workspace_bytes_for(T, H))
         return fail(MHC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, workspace_bytes_for(T, H));
@@ -510,6 +507,8 @@ mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *b
                           {layer_in_out, "layer_in_out"}, {pre_mix_out, "pre_mix_out"}, {post_mix_out, "post_mix_out"},
                           {comb_res_mix_out, "comb_res_mix_out"}})) != MHC_OK)
         return st;
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = mhc::launch_broadcast4(x, T, (int)H, residual_out, dev.sms, cs);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");

@@ -1,0 +1,99 @@
+"""CPU-only checks of the variant entry points (MXFP8 epilogue, int8 post, square-sum post,
+broadcast pre, side-stream split): their argument checks reject bad calls before touching
+CUDA, and the host-side size helpers hold their closed forms.  Pointers are fake aligned
+addresses: nothing is dereferenced before validation."""
+import ctypes
+
+import pytest
+
+import oracle
+
+SC = (2e-5, 2e-6, 1.25, 3e-4, 20)
+
+
+def P(a):
+    return ctypes.c_void_p(a)
+
+
+def ins(n, base=0x100000000):
+    return [P(base + i * (1 << 36)) for i in range(n)]
+
+
+def test_mxfp8_scale_bytes_matches_the_oracle_layout(mhc_lib):
+    L = mhc_lib.lib()
+    for T, H in [(1, 7168), (6, 7168), (128, 4096), (300, 7168 + 160), (8192, 7168)]:
+        rows, cols = oracle.mx_scale_shape(T, H)
+        assert L.mhc_mxfp8_scale_bytes(T, H) == rows * cols
+    assert L.mhc_mxfp8_scale_bytes(4, 1000) == 0      # H % 32 != 0
+
+
+def _mx_call(L, T, H, q, s, mode, X=True):
+    p = ins(8)
+    outs = ins(5, 0x200000000000)
+    return L.mhc_shifted_post_pre_mxfp8(*p, T, H, *SC[:4], SC[4], outs[0], outs[1] if X else None, q, s, mode,
+                                        outs[2], outs[3], outs[4], P(0x7000000000), 1 << 30, None)
+
+
+def test_mxfp8_argument_checks(mhc_lib):
+    L = mhc_lib.lib()
+    q, s = P(0x300000000000), P(0x310000000000)
+    assert _mx_call(L, 4, 1000, q, s, 0) == -1          # H % 32 != 0
+    assert _mx_call(L, 4, 1024, q, s, 2) == -1          # unknown scale rule
+    assert _mx_call(L, 4, 1024, None, s, 0) == -1       # no E4M3 buffer
+    assert _mx_call(L, 4, 1024, q, None, 0) == -1       # no scale buffer
+    assert _mx_call(L, 4, 1024, P(0x300000000004), s, 0) == -1   # misaligned E4M3 buffer
+    assert _mx_call(L, 0, 1024, q, s, 0) == 0           # T == 0: nothing to do
+
+
+def test_post_variant_argument_checks(mhc_lib):
+    L = mhc_lib.lib()
+    R, q, xs, pp, pc = ins(5)
+    out, ss = P(0x200000000000), P(0x210000000000)
+    assert L.mhc_post_int8(R, None, xs, pp, pc, 4, 1024, out, ss, None) == -1
+    assert L.mhc_post_int8(R, q, None, pp, pc, 4, 1024, out, ss, None) == -1
+    assert L.mhc_post_int8(R, q, xs, pp, pc, 4, 1020, out, ss, None) == -1       # H % 8
+    assert L.mhc_post_int8(R, q, xs, pp, pc, 4, 1024, out, R, None) == -1        # sqrsum overlaps R
+    assert L.mhc_post_sqrsum(R, q, pp, pc, 4, 1024, out, None, None) == -1       # sqrsum required
+    assert L.mhc_post_int8(R, q, xs, pp, pc, 0, 1024, out, ss, None) == 0
+
+
+def test_pre_broadcast_argument_checks(mhc_lib):
+    L = mhc_lib.lib()
+    x, phi, bias, ms, g = ins(5)
+    Ro, X, pre, post, res = ins(5, 0x200000000000)
+    ws = P(0x7000000000)
+    assert L.mhc_pre_broadcast(x, phi, bias, ms, g, 4, 1024, *SC[:4], SC[4], None, X, pre, post, res, ws,
+                               1 << 30, None) == -1                                # residual_out required
+    assert L.mhc_pre_broadcast(x, phi, bias, ms, g, 4, 1024, *SC[:4], SC[4], x, X, pre, post, res, ws,
+                               1 << 30, None) == -1                                # output overlaps x
+    assert L.mhc_pre_broadcast(x, phi, bias, ms, g, 4, 1024, *SC[:4], SC[4], Ro, Ro, pre, post, res, ws,
+                               1 << 30, None) == -1                                # outputs overlap
+    assert L.mhc_pre_broadcast(x, phi, bias, ms, g, 4, 1024, *SC[:4], SC[4], Ro, X, pre, post, res, ws,
+                               16, None) == -3                                     # workspace too small
+
+
+def test_split_argument_checks(mhc_lib):
+    L = mhc_lib.lib()
+    p = ins(8)
+    outs = ins(5, 0x200000000000)
+    ws = P(0x7000000000)
+    side, f, j = P(0x1234), P(0x5678), P(0x9abc)
+    common = (*p, 4, 1024, *SC[:4], SC[4], *outs, ws, 1 << 30)
+    assert L.mhc_shifted_post_pre_split(*common, None, side, None, j) == -1       # no fork event
+    assert L.mhc_shifted_post_pre_split(*common, None, side, f, None) == -1       # no join event
+    assert L.mhc_shifted_post_pre_split(*common, side, side, f, j) == -1          # side == main stream
+
+
+def test_bench_byte_counts_match_the_scope_table():
+    """The per-call algorithmic bytes: 20H + 176 per token plus phi (fp32 [4H, 24]), gamma and
+    the scalars per call: 3.63 MB for T=6 and 1.1786 GB for T=8192 at H=7168."""
+    import importlib.util
+    import os
+    spec = importlib.util.spec_from_file_location(
+        "bench", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert bench.algorithmic_bytes(6, 7168) == 6 * 143536 + 4 * 7168 * 24 * 4 + 2 * 7168 + 108
+    assert abs(bench.algorithmic_bytes(6, 7168) / 1e6 - 3.63) < 0.005
+    assert abs(bench.algorithmic_bytes(8192, 7168) / 1e9 - 1.1786) < 0.0001
+    assert bench.algorithmic_bytes(8192, 7168, True) - bench.algorithmic_bytes(8192, 7168) == 8192 * (7168 + 224)
