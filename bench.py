@@ -139,6 +139,18 @@ def dist_setup():
     return rank, ws, lr, dist
 
 
+def max_over_ranks(value, dist, device=None):
+    """The largest of the ranks' values (the job's time is its slowest rank's); the value itself
+    when there is one process."""
+    if dist is None:
+        return value
+    import torch
+    on_dev = device is not None and dist.get_backend() == "nccl"
+    t = torch.tensor([value], dtype=torch.float64, device=device if on_dev else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def time_oracle(w, phi, bias, ms, gamma, n_tokens, min_seconds, t_offset=0):
     """Times the CPU oracle over n_tokens tokens of the workload, repeated until
     min_seconds have passed.  Returns (tokens/s, threads, seconds, tokens)."""
@@ -365,10 +377,7 @@ def run_ours(args, rank, world, lr, dist):
         mhc.set_main_kernel_events(None, None)
     torch.cuda.synchronize(dev)
     kernel_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in kev]))
-    if dist is not None:
-        t = torch.tensor([el_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el_ms = float(t.item())
+    el_ms = max_over_ranks(el_ms, dist, dev)
     ms_step = el_ms / args.steps
     value = world * T / (ms_step / 1e3)
 
@@ -460,10 +469,7 @@ def run_ours(args, rank, world, lr, dist):
         e1.record(s_out)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     if rank != 0:
         return
