@@ -432,10 +432,18 @@ mhc_status mhc_shifted_post_pre_split(const mhc_bf16 *residual, const mhc_bf16 *
     }
     const mhc::SideStream side{static_cast<cudaStream_t>(side_stream), static_cast<cudaEvent_t>(fork_event),
                                static_cast<cudaEvent_t>(join_event)};
-    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
-                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
-                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
-                        comb_res_mix_out, workspace, workspace_bytes, stream, true, nullptr, nullptr, 0, &side);
+    const mhc_status st = run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                                       rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                                       sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                                       comb_res_mix_out, workspace, workspace_bytes, stream, true, nullptr, nullptr,
+                                       0, &side);
+    if (st == MHC_OK && T == 0) {  // nothing to compute: the events still mark the (empty) work done
+        cudaError_t e = cudaEventRecord(side.fork, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+        if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "event record");
+    }
+    return st;
 }
 
 size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H) {

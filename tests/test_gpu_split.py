@@ -113,3 +113,16 @@ def test_split_rejects_missing_events(mhc):
     assert rc == -1
     torch.cuda.synchronize()
     assert bool((o["layer_in"] == 7).all())
+
+
+def test_split_with_no_tokens_still_records_the_events(mhc):
+    H = 1024
+    args = inputs(1, H, 902)
+    e = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    z = (e(0, 4, H), e(0, H), torch.empty((0, 4), device="cuda"), torch.empty((0, 4, 4), device="cuda"), *args[4:])
+    side = torch.cuda.Stream()
+    f, j = torch.cuda.Event(), torch.cuda.Event()
+    o = mhc.shifted_post_pre_split(*z, **SC, side_stream=side, fork_event=f, join_event=j)
+    torch.cuda.current_stream().wait_event(j)
+    torch.cuda.synchronize()
+    assert o["layer_in"].shape == (0, H) and j.query()
