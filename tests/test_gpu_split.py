@@ -121,7 +121,7 @@ def test_split_with_no_tokens_still_records_the_events(mhc):
     e = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device="cuda")
     z = (e(0, 4, H), e(0, H), torch.empty((0, 4), device="cuda"), torch.empty((0, 4, 4), device="cuda"), *args[4:])
     side = torch.cuda.Stream()
-    f, j = torch.cuda.Event(), torch.cuda.Event()
+    f, j = events()
     o = mhc.shifted_post_pre_split(*z, **SC, side_stream=side, fork_event=f, join_event=j)
     torch.cuda.current_stream().wait_event(j)
     torch.cuda.synchronize()
