@@ -189,7 +189,9 @@ MHC_API size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H);
  *   scale_mode        MHC_MX_SCALE_FLOOR or MHC_MX_SCALE_CEIL; E is clamped to [-127, 127],
  *                     and an all-zero block gets E = -127
  * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  Runs on the ws and small schedules
- * (AUTO picks one of them); a forced other schedule returns MHC_ERR_UNSUPPORTED.  The bf16
+ * (AUTO picks one of them); a forced other schedule returns MHC_ERR_UNSUPPORTED.  On ws with
+ * layer_in_out given, the quantize is a second streaming pass over the bf16 layer input (the
+ * same bits; cheaper there than the in-kernel epilogue).  The bf16
  * output and the mixes are bit-identical to mhc_shifted_post_pre's on the same schedule. */
 MHC_API mhc_status mhc_shifted_post_pre_mxfp8(
     const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,

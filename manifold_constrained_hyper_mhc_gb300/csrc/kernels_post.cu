@@ -87,7 +87,42 @@ broadcast4_kernel(const uint16_t *__restrict__ x, int64_t n_vec, int nvec_row, i
     }
 }
 
+// The MXFP8 form of a bf16 layer input already in HBM: one thread per block of 32 values
+// (four 16-byte loads), the same quantize as the epilogues (mx_quantize_block).
+__global__ void __launch_bounds__(kPT)
+mx_quantize_kernel(const uint16_t *__restrict__ X, int64_t n_blk, int blk_row, int H, int mode,
+                   uint8_t *__restrict__ q, uint8_t *__restrict__ scale) {
+    // may start while the kernel before it (which wrote X) still runs: wait for its results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int64_t i = (int64_t)blockIdx.x * kPT + threadIdx.x; i < n_blk; i += (int64_t)gridDim.x * kPT) {
+        const int64_t t = i / blk_row;
+        const int k = (int)(i % blk_row);
+        const uint16_t *src = X + t * (int64_t)H + (int64_t)k * 32;
+        uint4 o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = ld_stream(src + 8 * j);
+        const int jj[4] = {0, 1, 2, 3};
+        mx_quantize_block(o, jj, mode, q + t * (int64_t)H + (int64_t)k * 32, scale + mx_scale_offset(t, k, H));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_mx_quantize(const uint16_t *X, int64_t T, int H, const MxOut &mx, int num_sms, cudaStream_t stream) {
+    const int blk_row = H / 32;
+    const int64_t n = T * blk_row;
+    const int64_t want = (n + kPT - 1) / kPT, cap = (int64_t)num_sms * 8;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap its launch with the tail before it
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(want < cap ? want : cap));
+    cfg.blockDim = dim3(kPT);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mx_quantize_kernel, X, n, blk_row, H, mx.mode, mx.q, mx.scale);
+}
 
 cudaError_t launch_broadcast4(const uint16_t *x, int64_t T, int H, uint16_t *R_out, int num_sms, cudaStream_t stream) {
     const int nvec = H / kVec;

@@ -314,9 +314,17 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.phi_pack = reinterpret_cast<uint4 *>(ws);
             float *zstash = reinterpret_cast<float *>(ws + ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)));
             a.C = 16; a.G = 8;
-            a.mx = mxo;
+            // with the bf16 layer input wanted as well, a separate streaming quantize pass over it
+            // is cheaper than ws's in-kernel epilogue (which lengthens the ring's critical chain);
+            // both give the same bits
+            const bool mx_pass = mx && layer_in_out != nullptr;
+            a.mx = mx_pass ? mhc::MxOut{nullptr, nullptr, 0} : mxo;
             e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
             g_launches = 2;
+            if (e == cudaSuccess && mx_pass) {
+                e = mhc::launch_mx_quantize(layer_in_out, T, (int)H, mxo, dev.sms, cs);
+                g_launches = 3;
+            }
             break;
         }
         case MHC_SCHEDULE_SMALL: {

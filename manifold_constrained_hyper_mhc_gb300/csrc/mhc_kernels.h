@@ -118,6 +118,9 @@ cudaError_t launch_post_ex(const uint16_t *R, const uint16_t *Y, const int8_t *Y
                            const float *prev_post, const float *prev_comb, int64_t T, int H, uint16_t *R_out,
                            float *sqrsum, cudaStream_t stream);
 
+// The MXFP8 form of a bf16 [T][H] layer input already written (kernels_post.cu); H % 32 == 0.
+cudaError_t launch_mx_quantize(const uint16_t *X, int64_t T, int H, const MxOut &mx, int num_sms, cudaStream_t stream);
+
 // R_out[t][j] = x[t] for the four streams (kernels_post.cu).
 cudaError_t launch_broadcast4(const uint16_t *x, int64_t T, int H, uint16_t *R_out, int num_sms, cudaStream_t stream);
 
