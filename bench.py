@@ -37,7 +37,7 @@ METRIC = "tokens/s and HBM GB/s (% of GB300 peak) for fused mHC post+pre vs T, H
 FALLBACK_HBM_GBS = 6800.0
 
 
-def algorithmic_bytes(T: int, H: int, mxfp8: bool = False) -> int:
+def algorithmic_bytes(T: int, H: int, mxfp8: bool = False, no_bf16: bool = False) -> int:
     """Bytes the op must move per call: per token R 8H + Y 2H + prev mixes 80 B in,
     R' 8H + layer input 2H + mixes 96 B out; per call phi (fp32 [4H, 24]) 384H + gamma 2H
     + bias and mix scales 108 B.  With the MXFP8 layer input: + H E4M3 bytes and H/32 scale
@@ -45,6 +45,8 @@ def algorithmic_bytes(T: int, H: int, mxfp8: bool = False) -> int:
     b = T * (20 * H + 176) + 384 * H + 2 * H + 108
     if mxfp8:
         b += T * (H + H // 32)
+    if no_bf16:
+        b -= T * 2 * H
     return b
 
 
@@ -233,6 +235,8 @@ def run_ours(args, rank, world, lr, dist):
     if mx_mode is not None:
         out["layer_in_fp8"] = torch.empty((T, H), dtype=torch.uint8, device=dev)
         out["layer_in_scales"] = torch.empty(mhc.mxfp8_scale_bytes(T, H), dtype=torch.uint8, device=dev)
+        if args.no_bf16:  # the MXFP8 layer input only
+            del out["layer_in"]
 
     xsd = None
     if args.op in ("post", "post_sqrsum", "post_int8"):
@@ -298,8 +302,9 @@ def run_ours(args, rank, world, lr, dist):
         elif mx_mode is None:
             mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=o, workspace=ws, stream=st)
         else:
-            mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode, out=o, workspace=ws,
-                                       stream=st)
+            mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode,
+                                       out=dict(o, layer_in=None) if args.no_bf16 else o, workspace=ws,
+                                       want_bf16=not args.no_bf16, stream=st)
 
     def step():
         call(Rd, Yd, ppd, pcd)
@@ -474,12 +479,13 @@ def run_ours(args, rank, world, lr, dist):
     if rank != 0:
         return
     peak, peak_src = peaks()
-    abytes = algorithmic_bytes(T, H, mx_mode is not None) if args.op in ("fused", "split") else \
+    abytes = algorithmic_bytes(T, H, mx_mode is not None, mx_mode is not None and args.no_bf16) \
+        if args.op in ("fused", "split") else \
         {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88),
          "pre_broadcast": T * (12 * H + 96) + 384 * H + 2 * H + 108}[args.op]
     # calls whose bytes are split over several kernels (the MXFP8 output written by a second
     # pass, the broadcast pre): the roofline uses the whole call's time
-    whole_call = mx_mode is not None or args.op == "pre_broadcast"
+    whole_call = (mx_mode is not None and not args.no_bf16) or args.op == "pre_broadcast"
     achieved = abytes / ((ms_step if whole_call else kernel_ms) / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
         {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op in ("fused", "split") else args.op
@@ -491,12 +497,14 @@ def run_ours(args, rank, world, lr, dist):
                    "op": {"fused": "mhc_shifted_post_pre", "post": "mhc_post", "post_sqrsum": "mhc_post_sqrsum",
                           "post_int8": "mhc_post_int8", "pre_broadcast": "mhc_pre_broadcast",
                           "split": "mhc_shifted_post_pre_split (mixes on a side stream)"}[args.op],
-                   "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)")
+                   "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)"
+                                                         + (", no bf16 layer input" if args.no_bf16 else ""))
                          + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
                    "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
                    "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": measured_traffic(sched if mx_mode is None else sched + "_mxfp8", w.name, T, H), "peak_source": peak_src,
+                     "traffic": None if whole_call else
+                     measured_traffic(sched if mx_mode is None else sched + "_mxfp8_only", w.name, T, H), "peak_source": peak_src,
                      "kernel": (f"whole call ({launches} launches), {ms_step * 1e3:.1f} us; main kernel "
                                 f"{kernel_ms * 1e3:.1f} us" if whole_call else
                                 f"main kernel of the call ({launches} launches per call), "
@@ -534,6 +542,7 @@ def main():
                     help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")
     ap.add_argument("--mxfp8", default="none", choices=["none", "floor", "ceil"],
                     help="also emit the layer input as MXFP8 (E4M3 + UE8M0 block scales)")
+    ap.add_argument("--no-bf16", action="store_true", help="with --mxfp8: the MXFP8 layer input only")
     args = ap.parse_args()
     rank, world, lr, dist = dist_setup()
     try:

@@ -87,22 +87,40 @@ broadcast4_kernel(const uint16_t *__restrict__ x, int64_t n_vec, int nvec_row, i
     }
 }
 
-// The MXFP8 form of a bf16 layer input already in HBM: one thread per block of 32 values
-// (four 16-byte loads), the same quantize as the epilogues (mx_quantize_block).
+// The MXFP8 form of a bf16 layer input already in HBM: a thread takes two blocks of 32 values
+// per step (eight 16-byte loads in flight), quantizes them as the epilogues do and stores each
+// block's 32 codes as two 16-byte stores.
 __global__ void __launch_bounds__(kPT)
 mx_quantize_kernel(const uint16_t *__restrict__ X, int64_t n_blk, int blk_row, int H, int mode,
                    uint8_t *__restrict__ q, uint8_t *__restrict__ scale) {
     // may start while the kernel before it (which wrote X) still runs: wait for its results
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int64_t i = (int64_t)blockIdx.x * kPT + threadIdx.x; i < n_blk; i += (int64_t)gridDim.x * kPT) {
-        const int64_t t = i / blk_row;
-        const int k = (int)(i % blk_row);
-        const uint16_t *src = X + t * (int64_t)H + (int64_t)k * 32;
-        uint4 o[4];
+    const int64_t stride = (int64_t)gridDim.x * kPT;
+    for (int64_t i0 = (int64_t)blockIdx.x * kPT + threadIdx.x; i0 < n_blk; i0 += 2 * stride) {
+        uint4 o[2][4];
+        int64_t t[2];
+        int k[2];
+        bool on[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = ld_stream(src + 8 * j);
-        const int jj[4] = {0, 1, 2, 3};
-        mx_quantize_block(o, jj, mode, q + t * (int64_t)H + (int64_t)k * 32, scale + mx_scale_offset(t, k, H));
+        for (int b = 0; b < 2; ++b) {
+            const int64_t i = i0 + b * stride;
+            on[b] = i < n_blk;
+            t[b] = on[b] ? i / blk_row : 0;
+            k[b] = on[b] ? (int)(i % blk_row) : 0;
+            const uint16_t *src = X + t[b] * (int64_t)H + (int64_t)k[b] * 32;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[b][j] = on[b] ? ld_stream(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            if (!on[b]) continue;
+            uint32_t w[8];
+            const uint8_t sb = mx_quantize_block32(o[b], mode, w);
+            uint4 *dst = reinterpret_cast<uint4 *>(q + t[b] * (int64_t)H + (int64_t)k[b] * 32);
+            __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+            __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+            scale[mx_scale_offset(t[b], k[b], H)] = sb;
+        }
     }
 }
 

@@ -214,10 +214,9 @@ __device__ __forceinline__ void mx_quantize8(uint4 o, bool active, int mode, uin
     if (((threadIdx.x & 31) & 3) == 0) *scale_dst = (uint8_t)(E + 127);
 }
 
-// One block of 32 held by one lane as four vectors o[k] (vector j[k] of the block, any
-// order): E4M3 codes to q_block + 8 * j[k], scale byte to *scale_dst.
-__device__ __forceinline__ void mx_quantize_block(const uint4 (&o)[4], const int (&j)[4], int mode,
-                                                  uint8_t *q_block, uint8_t *scale_dst) {
+// One block of 32 as four vectors o[0..3]: its 32 E4M3 codes in 8 words (vector k in words
+// 2k, 2k + 1) and, returned, the scale byte.
+__device__ __forceinline__ uint8_t mx_quantize_block32(const uint4 (&o)[4], int mode, uint32_t (&w)[8]) {
     float x[4][8];
     float amax = 0.f;
 #pragma unroll
@@ -227,18 +226,30 @@ __device__ __forceinline__ void mx_quantize_block(const uint4 (&o)[4], const int
         for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[k][e]));
     }
     const int E = mx_exp(amax, mode);
-    const float m = __uint_as_float((uint32_t)(127 - E) << 23);  // 2^-E (E <= 120 for finite bf16)
+    const float m = __uint_as_float((uint32_t)(127 - E) << 23);
     const float2 m2 = make_float2(m, m);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        uint32_t w[4];
+        uint32_t h[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
-            w[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(__fmul2_rn(make_float2(x[k][2 * p], x[k][2 * p + 1]), m2),
+            h[p] = (uint32_t)__nv_cvt_float2_to_fp8x2(__fmul2_rn(make_float2(x[k][2 * p], x[k][2 * p + 1]), m2),
                                                        __NV_SATFINITE, __NV_E4M3);
-        __stcs(reinterpret_cast<uint2 *>(q_block + 8 * j[k]), make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
+        w[2 * k] = h[0] | (h[1] << 16);
+        w[2 * k + 1] = h[2] | (h[3] << 16);
     }
-    *scale_dst = (uint8_t)(E + 127);
+    return (uint8_t)(E + 127);
+}
+
+// One block of 32 held by one lane as four vectors o[k] (vector j[k] of the block, any
+// order): E4M3 codes to q_block + 8 * j[k], scale byte to *scale_dst.
+__device__ __forceinline__ void mx_quantize_block(const uint4 (&o)[4], const int (&j)[4], int mode,
+                                                  uint8_t *q_block, uint8_t *scale_dst) {
+    uint32_t w[8];
+    const uint8_t sb = mx_quantize_block32(o, mode, w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) __stcs(reinterpret_cast<uint2 *>(q_block + 8 * j[k]), make_uint2(w[2 * k], w[2 * k + 1]));
+    *scale_dst = sb;
 }
 
 // ---- step (3): heads and Sinkhorn, one warp per token -----------------------
