@@ -256,6 +256,9 @@ def run_ours(args, rank, world, lr, dist):
     if args.op == "pre_broadcast":
         out = {"residual_out": out["residual_out"], "layer_in": out["layer_in"], "pre_mix": out["pre_mix"],
                "post_mix": out["post_mix"], "comb_res_mix": out["comb_res_mix"]}
+    if args.op == "pre":  # the pre alone (non-shift order): R plays the post-updated streams
+        out = {"layer_in": out["layer_in"], "pre_mix": out["pre_mix"], "post_mix": out["post_mix"],
+               "comb_res_mix": out["comb_res_mix"]}
 
     if args.op == "split":
         # two workspaces and event pairs: call i waits on the join of call i-2, so the side
@@ -289,6 +292,8 @@ def run_ours(args, rank, world, lr, dist):
                 st.wait_event(j_)
             mhc.shifted_post_pre_split(R_, Y_, pp_, pc_, *wd, **sc, side_stream=side, fork_event=f_, join_event=j_,
                                        out=o, workspace=wss[i % 2], stream=st)
+        elif args.op == "pre":
+            mhc.pre(R_, *wd, **sc, out=o, workspace=ws, stream=st)
         elif args.op == "pre_broadcast":  # the first layer: Y plays the (T, H) input  # the first layer: Y plays the (T, H) input
             mhc.pre_broadcast(Y_, *wd, **sc, out=o, workspace=ws, stream=st)
         elif args.op == "post":
@@ -482,20 +487,22 @@ def run_ours(args, rank, world, lr, dist):
     abytes = algorithmic_bytes(T, H, mx_mode is not None, mx_mode is not None and args.no_bf16) \
         if args.op in ("fused", "split") else \
         {"post": T * (18 * H + 80), "post_sqrsum": T * (18 * H + 84), "post_int8": T * (17 * H + 88),
+         "pre": T * (10 * H + 96) + 384 * H + 2 * H + 108,
          "pre_broadcast": T * (12 * H + 96) + 384 * H + 2 * H + 108}[args.op]
     # calls whose bytes are split over several kernels (the MXFP8 output written by a second
     # pass, the broadcast pre): the roofline uses the whole call's time
     whole_call = (mx_mode is not None and not args.no_bf16) or args.op == "pre_broadcast"
     achieved = abytes / ((ms_step if whole_call else kernel_ms) / 1e3) / 1e9
     sched = args.schedule if args.schedule != "auto" else \
-        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op in ("fused", "split") else args.op
+        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op in ("fused", "split", "pre") \
+        else args.op
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name} T={T} H={H} hc_mult=4", "T": T, "H": H,
                    "op": {"fused": "mhc_shifted_post_pre", "post": "mhc_post", "post_sqrsum": "mhc_post_sqrsum",
-                          "post_int8": "mhc_post_int8", "pre_broadcast": "mhc_pre_broadcast",
+                          "post_int8": "mhc_post_int8", "pre": "mhc_pre", "pre_broadcast": "mhc_pre_broadcast",
                           "split": "mhc_shifted_post_pre_split (mixes on a side stream)"}[args.op],
                    "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)"
                                                          + (", no bf16 layer input" if args.no_bf16 else ""))
@@ -536,7 +543,7 @@ def main():
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--op", default="fused",
-                    choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre_broadcast"],
+                    choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre", "pre_broadcast"],
                     help="the fused step (default) or one of the post-only entry points")
     ap.add_argument("--graph", type=int, default=0,
                     help="capture this many calls into a CUDA graph and time its replays (launch-bound sizes)")
