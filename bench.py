@@ -507,7 +507,7 @@ def run_ours(args, rank, world, lr, dist):
                    "io": "bf16 streams, fp32 mixes" + ("" if mx_mode is None else f", + MXFP8 layer input ({args.mxfp8} scales)"
                                                          + (", no bf16 layer input" if args.no_bf16 else ""))
                          + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
-                   "schedule": sched, "l2": "inputs larger than L2 (1.18 GB moved per call)",
+                   "schedule": sched, "l2": f"inputs larger than L2 ({abytes / 1e9:.2f} GB moved per call)",
                    "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if whole_call else

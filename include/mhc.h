@@ -103,9 +103,12 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_WS = 8,          /* as PIPE with warp-specialised roles (TMA producer, post,
                                      projection + Gram on the tensor cores, owner, combine) handing
                                      groups over through mbarriers, and a 6-deep tile ring */
-    MHC_SCHEDULE_SMALL = 9        /* T <= 64 only: one cooperative launch, one CTA per hidden slice
+    MHC_SCHEDULE_SMALL = 9,       /* T <= 64 only: one cooperative launch, one CTA per hidden slice
                                      on up to every SM, one bounded grid barrier between the partial
                                      sums and the combine (latency-bound decode calls) */
+    MHC_SCHEDULE_BCAST = 10       /* mhc_pre_broadcast only (H % 64 == 0): one persistent kernel that
+                                     works from x alone, 8 tokens per tile, x read twice (the second
+                                     time from L2); the other calls choose as AUTO */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */
@@ -266,8 +269,14 @@ MHC_API mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const flo
  * broadcast to the four streams ("[DSv4.1] Integrate Mega-mHC from DeepGEMM", "Paths on current
  * main that still call DeepGEMM on SM12x" item 1, mhc_pre_broadcast; the None pre mix of "Nit"
  * 6 only occurs here).  Writes residual_out [T,4,H] = four copies of x (what the next layer's
- * post reads), then computes steps (2)-(4) on it exactly as mhc_pre does (same outputs,
- * bit-identical to mhc_pre on that residual).  x must not overlap any output. */
+ * post reads) and steps (2)-(4) of that residual.  Two paths:
+ *   - T > 32 with H % 64 == 0 (or MHC_SCHEDULE_BCAST forced): one kernel that works from x
+ *     alone (phi summed over the four streams, x read twice, the second time from L2; 12H bytes
+ *     of HBM traffic per token).  Its results match the oracle within the usual tolerances but
+ *     are not bit-identical to mhc_pre's (another summation order);
+ *   - otherwise (or with another schedule forced): the residual is written first and mhc_pre
+ *     runs on it, bit-identical to mhc_pre on that residual.
+ * x must not overlap any output. */
 MHC_API mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *bias,
                                      const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T,
                                      int64_t H, float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,

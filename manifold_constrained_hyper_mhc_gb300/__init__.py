@@ -26,7 +26,7 @@ MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 OK = 0
 STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
           -4: "MHC_ERR_CUDA", -5: "MHC_ERR_DEVICE_TIMEOUT"}
-SCHEDULES = {"auto": 0, "split": 1, "cluster": 2, "cluster_8x16": 3, "cluster_8x8": 4, "cluster16": 5, "pipe": 6, "pipe2": 7, "ws": 8, "small": 9}
+SCHEDULES = {"auto": 0, "split": 1, "cluster": 2, "cluster_8x16": 3, "cluster_8x8": 4, "cluster16": 5, "pipe": 6, "pipe2": 7, "ws": 8, "small": 9, "bcast": 10}
 
 
 class MhcError(RuntimeError):
@@ -311,7 +311,9 @@ def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm
 def pre_broadcast(x, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,
                   sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None):
     """mhc_pre_broadcast: the first layer's pre from the (T, H) input x.  Returns the dict of
-    pre() plus residual_out [T,4,H] (four copies of x)."""
+    pre() plus residual_out [T,4,H] (four copies of x).  For T > 32 with H % 64 == 0 (or the
+    "bcast" schedule forced) one kernel works from x alone; otherwise the residual is written
+    and pre() runs on it."""
     T, H = x.shape
     _bf16(x, "x", (T, H))
     _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))

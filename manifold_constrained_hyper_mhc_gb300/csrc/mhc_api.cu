@@ -129,6 +129,7 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
         sched = std::max(sched, ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe2_stash_bytes(T));
         sched = std::max(sched, ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::ws_stash_bytes(T));
         sched = std::max(sched, mhc::small_workspace_bytes(T, (int)H));
+        sched = std::max(sched, mhc::bcast_workspace_bytes(T, H));
     }
     size_t b = mhc::kControlBytes + sched;
     return (b + 255) & ~size_t(255);
@@ -146,7 +147,8 @@ int auto_schedule(int64_t T, int64_t H, int sms, bool mx = false) {
 
 int choose_schedule(int64_t T, int64_t H, int sms, bool mx) {
     const int forced = g_forced_schedule.load(std::memory_order_relaxed);
-    if (forced != MHC_SCHEDULE_AUTO) return forced;
+    // the broadcast schedule only concerns mhc_pre_broadcast; the other calls choose as AUTO
+    if (forced != MHC_SCHEDULE_AUTO && forced != MHC_SCHEDULE_BCAST) return forced;
     return auto_schedule(T, H, sms, mx);
 }
 
@@ -523,9 +525,28 @@ mhc_status mhc_pre_broadcast(const mhc_bf16 *x, const float *phi, const float *b
                           {layer_in_out, "layer_in_out"}, {pre_mix_out, "pre_mix_out"}, {post_mix_out, "post_mix_out"},
                           {comb_res_mix_out, "comb_res_mix_out"}})) != MHC_OK)
         return st;
+    const int forced = g_forced_schedule.load(std::memory_order_relaxed);
+    const bool fusable = mhc::bcast_supported(T, H);
+    if (forced == MHC_SCHEDULE_BCAST && !fusable)
+        return fail(MHC_ERR_UNSUPPORTED, "the broadcast schedule needs H %% 64 == 0 (H=%lld)", (long long)H);
     Device dev;
     if ((st = current_device(dev)) != MHC_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the fused kernel from x alone, for all but the small-T calls (there the small schedule's
+    // one launch over every SM is faster than one CTA per 8 tokens)
+    if (forced == MHC_SCHEDULE_BCAST || (forced == MHC_SCHEDULE_AUTO && fusable && T > kSmallAutoMaxT)) {
+        mhc::BcastArgs a{};
+        a.x = x; a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
+        a.T = T; a.H = (int)H;
+        a.s = mhc::Scalars{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
+        a.R_out = residual_out; a.X_out = layer_in_out;
+        a.pre_out = pre_mix_out; a.post_out = post_mix_out; a.res_out = comb_res_mix_out;
+        cudaError_t e = mhc::launch_bcast_pre(a, static_cast<unsigned int *>(workspace),
+                                              static_cast<char *>(workspace) + mhc::kControlBytes, dev.sms, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        g_launches = 2;
+        return MHC_OK;
+    }
     cudaError_t e = mhc::launch_broadcast4(x, T, (int)H, residual_out, dev.sms, cs);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     st = run_post_pre(residual_out, nullptr, nullptr, nullptr, phi, bias, mix_scales, rmsnorm_weight, T, H,
@@ -622,7 +643,7 @@ mhc_status mhc_post_sqrsum(const mhc_bf16 *residual, const mhc_bf16 *layer_out, 
 mhc_status mhc_set_schedule(int schedule) {
     if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER16 &&
         schedule != MHC_SCHEDULE_PIPE && schedule != MHC_SCHEDULE_PIPE2 && schedule != MHC_SCHEDULE_WS &&
-        schedule != MHC_SCHEDULE_SMALL &&
+        schedule != MHC_SCHEDULE_SMALL && schedule != MHC_SCHEDULE_BCAST &&
         geom_of(schedule) == nullptr)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);

@@ -124,6 +124,23 @@ cudaError_t launch_mx_quantize(const uint16_t *X, int64_t T, int H, const MxOut 
 // R_out[t][j] = x[t] for the four streams (kernels_post.cu).
 cudaError_t launch_broadcast4(const uint16_t *x, int64_t T, int H, uint16_t *R_out, int num_sms, cudaStream_t stream);
 
+// The first layer's pre from its (T, H) input x, the residual being four copies of x
+// (kernels_bcast.cu): one packing launch, then one persistent kernel.
+struct BcastArgs {
+    const uint16_t *x;  // [T][H]
+    const float *phi, *bias, *mix_scales;
+    const uint16_t *gamma;
+    int64_t T;
+    int H;
+    Scalars s;
+    uint16_t *R_out;  // [T][4][H]: four copies of x
+    uint16_t *X_out;
+    float *pre_out, *post_out, *res_out;
+};
+bool bcast_supported(int64_t T, int64_t H);
+size_t bcast_workspace_bytes(int64_t T, int64_t H);  // after the control block
+cudaError_t launch_bcast_pre(const BcastArgs &a, unsigned int *status, void *scratch, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_post(const uint16_t *R, const uint16_t *Y, const float *prev_post,
                         const float *prev_comb, int64_t T, int H, uint16_t *R_out, int num_sms,
                         cudaStream_t stream);
