@@ -493,9 +493,15 @@ def run_ours(args, rank, world, lr, dist):
     # pass, the broadcast pre): the roofline uses the whole call's time
     whole_call = (mx_mode is not None and not args.no_bf16) or args.op == "pre_broadcast"
     achieved = abytes / ((ms_step if whole_call else kernel_ms) / 1e3) / 1e9
-    sched = args.schedule if args.schedule != "auto" else \
-        {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?") if args.op in ("fused", "split", "pre") \
-        else args.op
+    auto_name = {v: k for k, v in mhc.SCHEDULES.items()}.get(mhc.auto_schedule(T, H), "?")
+    if args.schedule != "auto":
+        sched = args.schedule
+    elif args.op in ("fused", "split", "pre"):
+        sched = auto_name
+    elif args.op == "pre_broadcast":  # the fused kernel from x alone above 32 tokens, else residual + pre
+        sched = "bcast" if T > 32 and H % 64 == 0 else f"broadcast + {auto_name} pre"
+    else:
+        sched = args.op
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -540,7 +546,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small", "bcast"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--op", default="fused",
                     choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre", "pre_broadcast"],

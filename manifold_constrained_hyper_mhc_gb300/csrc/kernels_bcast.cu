@@ -48,7 +48,7 @@ constexpr int kTT = 8;                      // tokens per tile
 constexpr int kCW = 512;                    // hidden values per chunk
 constexpr int kCHB = kCW / 64;              // 64-wide blocks per chunk (one TMA box)
 constexpr int kChunkBytes = kTT * kCW * 2;  // 8 KB
-constexpr int kNCh = 16;                    // ring depth
+constexpr int kNCh = 6;                     // ring depth: a small ring leaves L1 to the fragment loads
 constexpr int kCons = 8;                    // projection / combine warps
 constexpr int kWProd = kCons, kWStore = kCons + 1;
 constexpr int kNT = (kCons + 2) * 32;
