@@ -401,7 +401,10 @@ def run_ours(args, rank, world, lr, dist):
     hR = torch.from_numpy(R.view(np.int16)).pin_memory()
     hY = torch.from_numpy(Y if Y.dtype == np.int8 else Y.view(np.int16)).pin_memory()
     hpp, hpc = torch.from_numpy(pp).pin_memory(), torch.from_numpy(pc).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hR, hY, hpp, hpc))
+    # the inputs this op reads: the pre alone takes the residual only, the broadcast pre the
+    # (T, H) input only (Y plays it), the rest the residual, the layer output and the mixes
+    need_R, need_Y, need_mix = args.op != "pre_broadcast", args.op != "pre", args.op not in ("pre", "pre_broadcast")
+    h2d = sum(t.numel() * t.element_size() for t, n in ((hR, need_R), (hY, need_Y), (hpp, need_mix), (hpc, need_mix)) if n)
     sets = []
     for _ in range(2):
         o2 = {k: torch.empty_like(v) for k, v in out.items()}
@@ -420,10 +423,13 @@ def run_ours(args, rank, world, lr, dist):
         if not (capturing and i < 2):  # inside a capture, only events recorded in it can be waited on
             s_in.wait_event(b_["ev_free"])        # step i-2 is done with this set
         with torch.cuda.stream(s_in):
-            b_["R"].view(torch.int16).copy_(hR, non_blocking=True)
-            b_["Y"].view(hY.dtype).copy_(hY, non_blocking=True)
-            b_["pp"].copy_(hpp, non_blocking=True)
-            b_["pc"].copy_(hpc, non_blocking=True)
+            if need_R:
+                b_["R"].view(torch.int16).copy_(hR, non_blocking=True)
+            if need_Y:
+                b_["Y"].view(hY.dtype).copy_(hY, non_blocking=True)
+            if need_mix:
+                b_["pp"].copy_(hpp, non_blocking=True)
+                b_["pc"].copy_(hpc, non_blocking=True)
         b_["ev_in"].record(s_in)
         stream.wait_event(b_["ev_in"])
         call(b_["R"], b_["Y"], b_["pp"], b_["pc"], stream, b_["out"])
