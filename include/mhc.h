@@ -103,7 +103,8 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_WS = 8,          /* as PIPE with warp-specialised roles (TMA producer, post,
                                      projection + Gram on the tensor cores, owner, combine) handing
                                      groups over through mbarriers, and a 6-deep tile ring */
-    MHC_SCHEDULE_SMALL = 9,       /* T <= 64 only: one cooperative launch, one CTA per hidden slice
+    MHC_SCHEDULE_SMALL = 9,       /* T <= 128 only (and its shared memory must fit: at H = 7168,
+                                     T <= 96): one cooperative launch, one CTA per hidden slice
                                      on up to every SM, one bounded grid barrier between the partial
                                      sums and the combine (latency-bound decode calls) */
     MHC_SCHEDULE_BCAST = 10       /* mhc_pre_broadcast only (H % 64 == 0): one persistent kernel that

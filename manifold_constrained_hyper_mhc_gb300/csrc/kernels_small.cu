@@ -1,6 +1,6 @@
 // Small-T schedule (schedule "small"): the whole mHC post+pre step in one
-// launch for decode-sized calls (T <= 64), built for latency rather than
-// bandwidth.
+// launch for decode-sized calls (T <= 128 while the shared memory fits: eight 16-token
+// tiles for the eight warps of the projection), built for latency rather than bandwidth.
 //
 // The hidden dimension is split across up to one CTA per SM (slices of Hs
 // values, a multiple of 8; Hs = 64 at H = 7168, 112 CTAs).  CTA c:

@@ -101,7 +101,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
 
 // Small-T schedule (kernels_small.cu): one cooperative launch, one CTA per hidden slice,
 // one grid barrier on a 64-bit arrival counter at control-block bytes 64..71.
-constexpr int kSmallMaxT = 64;
+constexpr int kSmallMaxT = 128;
 int small_ctas(int H, int num_sms);
 int small_slice(int H, int num_sms, int align);  // align 8, or 32 for the MXFP8 output
 bool small_supported(int64_t T, int H, int num_sms, bool mx);
