@@ -72,6 +72,33 @@ def test_pre_broadcast_argument_checks(mhc_lib):
                                16, None) == -3                                     # workspace too small
 
 
+def test_broadcast_schedule_is_refused_where_it_cannot_run(mhc_lib):
+    """The fused broadcast schedule needs H % 64 == 0: forced on another H, mhc_pre_broadcast
+    refuses the call (MHC_ERR_UNSUPPORTED) before it touches the device.  The schedule id is
+    accepted, and the other calls treat it as AUTO."""
+    L = mhc_lib.lib()
+    x, phi, bias, ms, g = ins(5)
+    Ro, X, pre, post, res = ins(5, 0x200000000000)
+    ws = P(0x7000000000)
+    assert L.mhc_set_schedule(10) == 0
+    try:
+        assert L.mhc_pre_broadcast(x, phi, bias, ms, g, 40, 1032, *SC[:4], SC[4], Ro, X, pre, post, res, ws,
+                                   1 << 30, None) == -2
+    finally:
+        assert L.mhc_set_schedule(0) == 0
+    assert L.mhc_set_schedule(11) == -1                                           # unknown schedule
+
+
+def test_workspace_covers_the_broadcast_kernel(mhc_lib):
+    """The workspace holds the packed phi_sum fragments (96 bytes per hidden value, in 16-value
+    steps) and the residual-mix logits (64 bytes per token) after the 256-byte control block."""
+    L = mhc_lib.lib()
+    L.mhc_workspace_size.restype = ctypes.c_size_t
+    for T, H in [(33, 1024), (8192, 7168), (65536, 7168), (300, 1088)]:
+        need = 256 + (((H + 15) // 16 * 1536 + 255) // 256 * 256) + T * 64
+        assert L.mhc_workspace_size(T, H) >= need
+
+
 def test_split_argument_checks(mhc_lib):
     L = mhc_lib.lib()
     p = ins(8)
