@@ -86,6 +86,30 @@ def test_pre_broadcast_rejects_overlap_before_launching(mhc):
     assert bool((big.view(torch.int16) == 7).all())
 
 
+@pytest.mark.parametrize("T,H", [(8, 64), (41, 64), (16, 512), (152 * 8 + 3, 192)])
+def test_pre_broadcast_fused_edges(mhc, T, H):
+    """The fused kernel at its edges: H = 64 (one chunk mostly outside the tensor, zero-filled
+    loads and clipped stores), whole and ragged 8-token tiles, exactly one chunk, and more
+    tiles than CTAs with a ragged last tile."""
+    w = synth.Workload(f"bcast_edge_{T}x{H}", T, H, 900 + T, token_scale=True)
+    phi, bias, ms, gamma = synth.weights(w)
+    _, x, _, _ = synth.tokens(w)
+    mhc.set_schedule("bcast")
+    try:
+        ws = mhc.new_workspace(T, H)
+        o = mhc.pre_broadcast(dev(x), dev(phi), dev(bias), dev(ms), dev(gamma), **SC, workspace=ws)
+        mhc.check_status(ws)
+    finally:
+        mhc.set_schedule("auto")
+    ref = oracle.pre_broadcast(x, phi, bias, ms, gamma, **SC, debug=True)
+    assert np.array_equal(host_bf16(o["residual_out"]), ref["R"])
+    nb, mu, _ = bf16_check(host_bf16(o["layer_in"]), ref["X"], layer_in_floor(ref["R"], ref["pre"], ref["rstd"], gamma))
+    assert nb == 0, f"layer_in: {nb} bad, max {mu} ulp"
+    for k, rk in (("pre_mix", "pre"), ("post_mix", "post"), ("comb_res_mix", "res")):
+        d = np.abs(o[k].cpu().numpy().astype(np.float64) - ref[rk]).max()
+        assert d <= MIX_ATOL, (k, d)
+
+
 def test_pre_broadcast_fused_prefill_chunk_sampled(mhc):
     """The fused kernel at the prefill chunk's size (T = 8192, H = 7168), as the bench runs it:
     the residual is checked whole on the GPU, the other outputs on sampled tokens (the first and
