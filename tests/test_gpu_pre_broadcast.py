@@ -146,3 +146,30 @@ def test_pre_broadcast_auto_picks_fused_above_32(mhc, T):
     mhc.pre_broadcast(dev(x), dev(phi), dev(bias), dev(ms), dev(gamma), **SC)
     torch.cuda.synchronize()
     assert mhc.last_launch_count() == 2
+
+
+def test_pre_broadcast_fused_in_graph_capture_on_fresh_stream(mhc):
+    """The fused path (a packing launch, then the kernel under programmatic dependent launch)
+    captured into a CUDA graph on a new stream: the replay gives the eager result bit for bit."""
+    T, H = 300, 2048
+    w = synth.Workload("bcast_graph", T, H, 77)
+    phi, bias, ms, gamma = synth.weights(w)
+    _, x, _, _ = synth.tokens(w)
+    args = (dev(x), dev(phi), dev(bias), dev(ms), dev(gamma))
+    eager = mhc.pre_broadcast(*args, **SC)
+    torch.cuda.synchronize()
+    outs = {k: torch.empty_like(v) for k, v in eager.items()}
+    ws = mhc.new_workspace(T, H)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mhc.pre_broadcast(*args, **SC, out=outs, workspace=ws, stream=s)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in eager:
+        a, b = eager[k], outs[k]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), k
+    mhc.check_status(ws)
