@@ -91,9 +91,15 @@ def lib():
     return _lib
 
 
+_torch_mod = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+    return _torch_mod
 
 
 def _ptr(t):
@@ -122,11 +128,12 @@ def new_workspace(T: int, H: int, device=None):
     return torch.zeros(max(workspace_size(T, H), 256), dtype=torch.uint8, device=device or "cuda")
 
 
+# The checks below run on every call, so they stay cheap: a torch.Size compares equal to a tuple.
 def _bf16(t, name, shape):
     torch = _torch()
-    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+    if t.dtype != torch.bfloat16 and t.dtype != torch.int16 and t.dtype != torch.uint16:
         raise TypeError(f"{name} must be bfloat16 (or its 16-bit bit pattern), got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -137,7 +144,7 @@ def _f32(t, name, shape):
     torch = _torch()
     if t.dtype != torch.float32:
         raise TypeError(f"{name} must be float32, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -145,14 +152,15 @@ def _f32(t, name, shape):
 
 
 def _outputs(T, H, device, out, with_residual):
+    """The output dict: the caller's tensors, and new ones only for the keys it left out."""
     torch = _torch()
     out = dict(out or {})
-    if with_residual:
-        out.setdefault("residual_out", torch.empty((T, 4, H), dtype=torch.bfloat16, device=device))
-    out.setdefault("layer_in", torch.empty((T, H), dtype=torch.bfloat16, device=device))
-    out.setdefault("pre_mix", torch.empty((T, 4), dtype=torch.float32, device=device))
-    out.setdefault("post_mix", torch.empty((T, 4), dtype=torch.float32, device=device))
-    out.setdefault("comb_res_mix", torch.empty((T, 4, 4), dtype=torch.float32, device=device))
+    shapes = ((("residual_out", (T, 4, H), torch.bfloat16),) if with_residual else ()) + (
+        ("layer_in", (T, H), torch.bfloat16), ("pre_mix", (T, 4), torch.float32),
+        ("post_mix", (T, 4), torch.float32), ("comb_res_mix", (T, 4, 4), torch.float32))
+    for k, shape, dtype in shapes:
+        if k not in out:
+            out[k] = torch.empty(shape, dtype=dtype, device=device)
     return out
 
 
@@ -228,8 +236,10 @@ def shifted_post_pre_mxfp8(residual, layer_out, prev_post_mix, prev_comb_res_mix
     if not want_bf16:
         o.setdefault("layer_in", None)
     o = _outputs(T, H, dev, o, True)
-    o.setdefault("layer_in_fp8", torch.empty((T, H), dtype=torch.uint8, device=dev))
-    o.setdefault("layer_in_scales", torch.empty(max(mxfp8_scale_bytes(T, H), 1), dtype=torch.uint8, device=dev))
+    if "layer_in_fp8" not in o:
+        o["layer_in_fp8"] = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    if "layer_in_scales" not in o:
+        o["layer_in_scales"] = torch.empty(max(mxfp8_scale_bytes(T, H), 1), dtype=torch.uint8, device=dev)
     ws = workspace if workspace is not None else new_workspace(T, H, dev)
     rc = lib().mhc_shifted_post_pre_mxfp8(
         _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
