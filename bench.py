@@ -75,12 +75,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
             self.proc = None
         return self
+
+    def wait_first(self, timeout=3.0):
+        """Blocks until the sampler has delivered a row (nvidia-smi takes a moment to start)."""
+        t0 = time.time()
+        while self.proc is not None and not self.rows and time.time() - t0 < timeout:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -225,6 +231,11 @@ def run_ours(args, rank, world, lr, dist):
           d_bf16(gamma))
     sc = synth.scalars()
     ws = mhc.new_workspace(T, H, dev)
+    # phi is a weight: packed once (mhc_pack_phi), as at model load, and the fused call and the pre
+    # take the packed form (mhc_*_prepacked, bit-identical to the plain calls); --pack-per-call
+    # times the plain calls, which pack phi in their workspace on every call
+    packed = mhc.pack_phi(wd[0]) if args.op in ("fused", "pre") and args.mxfp8 == "none" and not args.pack_per_call \
+        else None
     out = {"residual_out": torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev),
            "layer_in": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
            "pre_mix": torch.empty((T, 4), device=dev), "post_mix": torch.empty((T, 4), device=dev),
@@ -293,7 +304,7 @@ def run_ours(args, rank, world, lr, dist):
             mhc.shifted_post_pre_split(R_, Y_, pp_, pc_, *wd, **sc, side_stream=side, fork_event=f_, join_event=j_,
                                        out=o, workspace=wss[i % 2], stream=st)
         elif args.op == "pre":
-            mhc.pre(R_, *wd, **sc, out=o, workspace=ws, stream=st)
+            mhc.pre(R_, *wd, **sc, out=o, workspace=ws, stream=st, packed_phi=packed)
         elif args.op == "pre_broadcast":  # the first layer: Y plays the (T, H) input  # the first layer: Y plays the (T, H) input
             mhc.pre_broadcast(Y_, *wd, **sc, out=o, workspace=ws, stream=st)
         elif args.op == "post":
@@ -305,7 +316,7 @@ def run_ours(args, rank, world, lr, dist):
             mhc.lib().mhc_post_int8(*[mhc._ptr(x) for x in (R_, Y_, xsd, pp_, pc_)], T, H,
                                     mhc._ptr(o["residual_out"]), mhc._ptr(o["sqrsum"]), mhc._stream(st, dev))
         elif mx_mode is None:
-            mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=o, workspace=ws, stream=st)
+            mhc.shifted_post_pre(R_, Y_, pp_, pc_, *wd, **sc, out=o, workspace=ws, stream=st, packed_phi=packed)
         else:
             mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode,
                                        out=dict(o, layer_in=None) if args.no_bf16 else o, workspace=ws,
@@ -349,7 +360,15 @@ def run_ours(args, rank, world, lr, dist):
 
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    # clocks: the sampler runs through an untimed pre-roll of the same steps (about 0.3 s, so that
+    # it has samples under this load however short the timed region is) and the timed region
     with ClockSampler(dev.index) as clk:
+        clk.wait_first()
+        t_roll = time.perf_counter()
+        while time.perf_counter() - t_roll < 0.3:
+            run_steps()
+            torch.cuda.synchronize(dev)
+        barrier()
         ev0.record(stream)
         for _ in range(n_replay):
             run_steps()
@@ -520,6 +539,8 @@ def run_ours(args, rank, world, lr, dist):
                                                          + (", no bf16 layer input" if args.no_bf16 else ""))
                          + (", int8 layer output with per-token scales" if args.op == "post_int8" else ""),
                    "schedule": sched, "l2": f"inputs larger than L2 ({abytes / 1e9:.2f} GB moved per call)",
+                   "phi": "packed once before the timed region (mhc_pack_phi), the call takes the packed form"
+                          if packed is not None else "packed by every call in its workspace",
                    "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if whole_call else
@@ -534,7 +555,7 @@ def run_ours(args, rank, world, lr, dist):
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipelining": "two buffer sets; copies in, calls and copies out on three streams"},
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window="an untimed pre-roll of the same steps (~0.3 s) and the timed region"),
     }
     if world == 1 and not args.no_cpu_baseline:
         tps, nt, el, done = time_oracle(w, phi, bias, msc, gamma, min(1024, T), 10.0)
@@ -552,7 +573,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "cluster", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small", "bcast"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "ws", "small", "bcast"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--op", default="fused",
                     choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre", "pre_broadcast"],
@@ -562,6 +583,8 @@ def main():
     ap.add_argument("--mxfp8", default="none", choices=["none", "floor", "ceil"],
                     help="also emit the layer input as MXFP8 (E4M3 + UE8M0 block scales)")
     ap.add_argument("--no-bf16", action="store_true", help="with --mxfp8: the MXFP8 layer input only")
+    ap.add_argument("--pack-per-call", action="store_true",
+                    help="time the plain calls, which pack phi on every call, instead of the prepacked ones")
     args = ap.parse_args()
     rank, world, lr, dist = dist_setup()
     try:

@@ -49,9 +49,11 @@
  *     other overlap between an input and an output is rejected.
  *   - The workspace is caller-owned device memory of at least
  *     mhc_workspace_size(T, H) bytes, 256-byte aligned.  Before its first use it
- *     must be zero-filled (e.g. cudaMemsetAsync); every successful call leaves
- *     it zeroed-state-compatible again.  Calls that share one workspace must be
- *     ordered (same stream or explicit events); concurrent use races.
+ *     must be zero-filled (e.g. cudaMemsetAsync); every call that completes
+ *     leaves it ready for the next call, whatever that call's T and H (after a
+ *     device-side timeout, mhc_check_status clears it).  Calls that share one
+ *     workspace must be ordered (same stream or explicit events); concurrent
+ *     use races.
  */
 #ifndef MHC_H
 #define MHC_H
@@ -89,20 +91,18 @@ typedef enum mhc_status {
 /* Kernel schedules.  AUTO picks by T, H and the SM count. */
 typedef enum mhc_schedule {
     MHC_SCHEDULE_AUTO = 0,
-    MHC_SCHEDULE_SPLIT = 1,       /* three launches: post + partial sums, mixes, combine + RMSNorm */
-    MHC_SCHEDULE_CLUSTER = 2,     /* one pass over HBM, clusters split the hidden dim; default geometry */
-    MHC_SCHEDULE_CLUSTER_8x16 = 3,/* clusters of 8 CTAs, 16 tokens per group, 1 CTA per SM */
-    MHC_SCHEDULE_CLUSTER_8x8 = 4, /* clusters of 8 CTAs, 8 tokens per group, 2 CTAs per SM */
-    MHC_SCHEDULE_CLUSTER16 = 5,   /* clusters of 16 CTAs, 16 tokens per group, phi resident in
-                                     tensor memory, next group's rows fetched by bulk async copies */
-    MHC_SCHEDULE_PIPE = 6,        /* clusters of 16 CTAs, 8 tokens per group, TMA tensor copies into a
-                                     triple buffer, point-to-point DSMEM messages, no cluster barrier
-                                     in the steady state */
-    MHC_SCHEDULE_PIPE2 = 7,       /* as PIPE, with the projection on tcgen05.mma (phi resident in
-                                     tensor memory as the A operand) and the Sinkhorn batched at the end */
-    MHC_SCHEDULE_WS = 8,          /* as PIPE with warp-specialised roles (TMA producer, post,
-                                     projection + Gram on the tensor cores, owner, combine) handing
-                                     groups over through mbarriers, and a 6-deep tile ring */
+    MHC_SCHEDULE_SPLIT = 1,       /* three launches: post + partial sums, mixes, combine + RMSNorm
+                                     (any H; AUTO's choice where ws does not fit, H > 7168) */
+    /* values 2-7 named cluster and pipelined schedules that the ws schedule superseded; they
+       were removed and mhc_set_schedule rejects them */
+    MHC_SCHEDULE_WS = 8,          /* clusters of 16 CTAs split the hidden dimension (H <= 7168), 8
+                                     tokens per group, phi resident in tensor memory; warp-specialised
+                                     roles (post, projection + Gram on the tensor cores, owner,
+                                     combine) hand groups over through mbarriers, TMA tensor copies
+                                     into a 6-deep tile ring, point-to-point DSMEM messages; a
+                                     second small launch redoes the layer input of tokens whose
+                                     streams cancel in X with a direct square sum (it exits at once
+                                     when there are none) */
     MHC_SCHEDULE_SMALL = 9,       /* T <= 128 only (and its shared memory must fit: at H = 7168,
                                      T <= 96): one cooperative launch, one CTA per hidden slice
                                      on up to every SM, one bounded grid barrier between the partial
@@ -222,8 +222,11 @@ MHC_API mhc_status mhc_shifted_post_pre_mxfp8(
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
  *   - Every call on a device shares the one array, which keeps the previous
- *     call's contents; nothing in it needs clearing between calls.  Calls that
- *     overlap on the GPU (different streams without ordering) race on it.
+ *     call's contents; nothing in it needs clearing between calls, whatever
+ *     their T and H.  Calls that overlap on the GPU (different streams without
+ *     ordering) race on it.
+ *   - A bounded device-side wait that gives up sets the array's status word:
+ *     mhc_noalloc_check_status reads and clears it.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 MHC_API mhc_status mhc_shifted_post_pre_noalloc(
     const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
@@ -232,6 +235,14 @@ MHC_API mhc_status mhc_shifted_post_pre_noalloc(
     float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
     void *stream);
+
+/* The allocation-free counterpart of mhc_check_status (the pages have no counterpart of it
+ * either): synchronises `stream`, then reads the status word of the static scratch that
+ * mhc_shifted_post_pre_noalloc uses on the current device.  MHC_ERR_DEVICE_TIMEOUT if a bounded
+ * device-side wait of one of those calls gave up since the last check (the call's outputs are
+ * then not to be trusted); it then zero-fills the scratch's control block, so later calls work
+ * again.  MHC_ERR_CUDA if the stream reports an error, else MHC_OK.  Allocates nothing. */
+MHC_API mhc_status mhc_noalloc_check_status(void *stream);
 
 /* Step (1) alone: the mHC post ("[SM80] Backport mHC fused post + int8
  * all-reduce", "What this fixes").  Needs no workspace. */
@@ -265,6 +276,37 @@ MHC_API mhc_status mhc_pre(const mhc_bf16 *residual, const float *phi, const flo
                    float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *layer_in_out,
                    float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* phi in the packed form the fused kernels read, made once per weight instead of on every call
+ * ("[DSv4.1] Integrate Mega-mHC from DeepGEMM", "Paths on current main that still call DeepGEMM
+ * on SM12x" item 1: the hc prenorm GEMM over the flattened hc_mult * hidden row, whose weight
+ * phi is constant across calls).  The packed form holds phi^T split into a bf16 high part and a
+ * bf16 remainder, in the fragment order of the tensor-core projection; a plain call rebuilds it
+ * in its workspace each time (one extra launch).
+ *   mhc_packed_phi_bytes(H)  bytes of the packed form (0 for an H the library does not take)
+ *   mhc_pack_phi             writes it from phi [4H,24] fp32 into packed_phi (caller-owned device
+ *                            memory of at least that many bytes, 16-byte aligned, not
+ *                            overlapping phi) on `stream`; asynchronous, one launch
+ * The _prepacked calls take the packed form next to phi (packed_phi must be mhc_pack_phi's output
+ * for this phi and H, and must not be written while a call that reads it runs); everything else
+ * is as in mhc_shifted_post_pre / mhc_pre, and the results are bit-identical to theirs.  Schedules
+ * that read phi directly (small, split) ignore packed_phi. */
+MHC_API size_t mhc_packed_phi_bytes(int64_t H);
+MHC_API mhc_status mhc_pack_phi(const float *phi, int64_t H, void *packed_phi, size_t packed_bytes, void *stream);
+MHC_API mhc_status mhc_shifted_post_pre_prepacked(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const void *packed_phi, const float *bias,
+    const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps,
+    float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+    void *workspace, size_t workspace_bytes, void *stream);
+MHC_API mhc_status mhc_pre_prepacked(const mhc_bf16 *residual, const float *phi, const void *packed_phi,
+                                     const float *bias, const float *mix_scales, const mhc_bf16 *rmsnorm_weight,
+                                     int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps,
+                                     float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters,
+                                     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                                     float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /* The first layer's pre: the residual does not exist yet and the layer's (T, H) input x is
  * broadcast to the four streams ("[DSv4.1] Integrate Mega-mHC from DeepGEMM", "Paths on current

@@ -20,13 +20,14 @@ __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
     "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
     "post_int8", "post_sqrsum", "pre_broadcast", "shifted_post_pre_split", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
+    "packed_phi_bytes", "pack_phi",
 ]
 MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 
 OK = 0
 STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
           -4: "MHC_ERR_CUDA", -5: "MHC_ERR_DEVICE_TIMEOUT"}
-SCHEDULES = {"auto": 0, "split": 1, "cluster": 2, "cluster_8x16": 3, "cluster_8x8": 4, "cluster16": 5, "pipe": 6, "pipe2": 7, "ws": 8, "small": 9, "bcast": 10}
+SCHEDULES = {"auto": 0, "split": 1, "ws": 8, "small": 9, "bcast": 10}
 
 
 class MhcError(RuntimeError):
@@ -69,6 +70,15 @@ def lib():
             L.mhc_shifted_post_pre_split.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
                                                      P, P, P, P, P, P, Z, P, P, P, P]
             L.mhc_shifted_post_pre_split.restype = I
+            L.mhc_packed_phi_bytes.argtypes = [I64]
+            L.mhc_packed_phi_bytes.restype = Z
+            L.mhc_pack_phi.argtypes = [P, I64, P, Z, P]
+            L.mhc_pack_phi.restype = I
+            L.mhc_shifted_post_pre_prepacked.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
+                                                         P, P, P, P, P, P, Z, P]
+            L.mhc_shifted_post_pre_prepacked.restype = I
+            L.mhc_pre_prepacked.argtypes = [P, P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
+            L.mhc_pre_prepacked.restype = I
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -164,12 +174,30 @@ def _outputs(T, H, device, out, with_residual):
     return out
 
 
+def packed_phi_bytes(H: int) -> int:
+    return int(lib().mhc_packed_phi_bytes(int(H)))
+
+
+def pack_phi(phi, *, out=None, stream=None):
+    """mhc_pack_phi: phi [4H, 24] fp32 in the packed form the fused kernels read (a uint8 tensor of
+    packed_phi_bytes(H) bytes), for the packed_phi argument of shifted_post_pre and pre."""
+    torch = _torch()
+    H = phi.shape[0] // 4
+    _f32(phi, "phi", (4 * H, 24))
+    n = packed_phi_bytes(H)
+    o = out if out is not None else torch.empty(max(n, 16), dtype=torch.uint8, device=phi.device)
+    _check(lib().mhc_pack_phi(_ptr(phi), H, _ptr(o), o.numel() * o.element_size(), _stream(stream, phi.device)),
+           "mhc_pack_phi")
+    return o
+
+
 def shifted_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
                      rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
-                     sinkhorn_iters=20, out=None, workspace=None, stream=None):
+                     sinkhorn_iters=20, out=None, workspace=None, stream=None, packed_phi=None):
     """mhc_shifted_post_pre: the fused post+pre step.  Returns a dict with
     residual_out [T,4,H] bf16, layer_in [T,H] bf16, pre_mix [T,4], post_mix [T,4],
-    comb_res_mix [T,4,4] (fp32).  ``out`` may supply preallocated outputs."""
+    comb_res_mix [T,4,4] (fp32).  ``out`` may supply preallocated outputs; with ``packed_phi``
+    (pack_phi(phi)) it calls mhc_shifted_post_pre_prepacked (same results, no packing launch)."""
     T, _, H = residual.shape
     _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
     _f32(prev_post_mix, "prev_post_mix", (T, 4)); _f32(prev_comb_res_mix, "prev_comb_res_mix", (T, 4, 4))
@@ -178,6 +206,15 @@ def shifted_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi,
     dev = residual.device
     o = _outputs(T, H, dev, out, True)
     ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    if packed_phi is not None:
+        rc = lib().mhc_shifted_post_pre_prepacked(
+            _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
+            _ptr(packed_phi), _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
+            hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
+            _ptr(o["pre_mix"]), _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
+            ws.numel() * ws.element_size(), _stream(stream, dev))
+        _check(rc, "mhc_shifted_post_pre_prepacked")
+        return o
     rc = lib().mhc_shifted_post_pre(
         _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
         _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
@@ -299,9 +336,9 @@ def post_sqrsum(residual, layer_out, prev_post_mix, prev_comb_res_mix, *, out=No
 
 
 def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale,
-        sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None):
+        sinkhorn_eps, sinkhorn_iters=20, out=None, workspace=None, stream=None, packed_phi=None):
     """mhc_pre: steps (2)-(4) from post-updated streams.  Returns the fused call's
-    outputs without residual_out."""
+    outputs without residual_out.  With ``packed_phi`` it calls mhc_pre_prepacked."""
     T, _, H = residual.shape
     _bf16(residual, "residual", (T, 4, H))
     _f32(phi, "phi", (4 * H, 24)); _f32(bias, "bias", (24,)); _f32(mix_scales, "mix_scales", (3,))
@@ -309,6 +346,14 @@ def pre(residual, phi, bias, mix_scales, rmsnorm_weight, *, hc_norm_eps, rmsnorm
     dev = residual.device
     o = _outputs(T, H, dev, out, False)
     ws = workspace if workspace is not None else new_workspace(T, H, dev)
+    if packed_phi is not None:
+        rc = lib().mhc_pre_prepacked(_ptr(residual), _ptr(phi), _ptr(packed_phi), _ptr(bias), _ptr(mix_scales),
+                                     _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale,
+                                     sinkhorn_eps, int(sinkhorn_iters), _ptr(o["layer_in"]), _ptr(o["pre_mix"]),
+                                     _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream, dev))
+        _check(rc, "mhc_pre_prepacked")
+        return o
     rc = lib().mhc_pre(_ptr(residual), _ptr(phi), _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight),
                        T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, int(sinkhorn_iters),
                        _ptr(o["layer_in"]), _ptr(o["pre_mix"]), _ptr(o["post_mix"]),

@@ -28,7 +28,9 @@
 // token chunk's) records of every CTA:
 //   heads [T][nc][16]: pre logits 0..3, Gram entries (0,0) (1,1) (2,2) (3,3)
 //                      (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), two zeros;
-//   tails [T][nc][24]: logits 4..23, four zeros.
+//   tails [T][nc][24]: logits 4..23, four zeros;
+//   then [T][nc] floats: each CTA's share of sum_h X^2 for tokens whose streams cancel in X
+//   (written and read only when gram_cancels flags a token).
 #include <cstdint>
 
 #include "mhc_device.cuh"
@@ -104,26 +106,30 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = pack2_rn(x0 - h0, x1 - h1);
 }
 
-// Grid barrier on a monotonic 64-bit arrival counter (zero before the first use;
-// every completed barrier leaves it at a multiple of the CTA count).  Release on
-// arrival, acquire on the poll.  Bounded in time: on a timeout it returns false.
-__device__ bool grid_barrier(unsigned long long *ctr, unsigned long long n) {
-    bool ok = true;
-    if (threadIdx.x == 0) {
-        unsigned long long old, cur;
-        asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
-        const unsigned long long target = (old / n + 1) * n;
-        const uint64_t t0 = globaltimer_ns();
-        while (true) {
-            asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(ctr) : "memory");
-            if (cur >= target) break;
-            if (globaltimer_ns() - t0 > kSpinLimitNs) {
-                ok = false;
-                break;
-            }
-        }
+// Grid barrier on one 64-bit word: the low 32 bits count the CTAs that have arrived, the high
+// 32 bits count the barriers completed on this word.  Called by one thread of each of the n CTAs.
+// Every CTA adds 1 (release); the CTA whose add makes the count n is the last, and it then adds
+// 2^32 - n, which returns the count to zero and advances the generation in one atomic.  A CTA
+// waits (acquire) until it sees either the count equal to n or the generation moved, so the barrier
+// opens as soon as the last arrival lands, and the reset is off that path.  A completed barrier
+// leaves the count at zero whatever n was, so calls with different CTA counts (different H) can
+// share the word; within one launch each barrier has its own word (a CTA may arrive at the next
+// barrier before the last one's reset of the previous one lands).  Bounded in time: on a
+// timeout it returns false; the CTA has still arrived, so the word stays consistent.
+__device__ bool grid_barrier(unsigned long long *word, unsigned int n) {
+    unsigned long long old, cur;
+    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(word) : "memory");
+    if ((unsigned int)(old & 0xFFFFFFFFull) == n - 1u) {
+        const unsigned long long step = (1ull << 32) - n;
+        asm volatile("red.add.relaxed.gpu.u64 [%0], %1;" ::"l"(word), "l"(step) : "memory");
     }
-    return ok;
+    const unsigned int gen = (unsigned int)(old >> 32);
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(word) : "memory");
+        if ((unsigned int)(cur & 0xFFFFFFFFull) == n || (unsigned int)(cur >> 32) != gen) return true;
+        if (globaltimer_ns() - t0 > kSpinLimitNs) return false;
+    }
 }
 
 // Warp-wide sum over the CTAs of 16 adjacent values, src[q * stride + 0..15] for CTA
@@ -197,6 +203,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
 
     // ---- bulk copies: mixes + gamma (barrier 0), phi slice rows j*H + h0 .. (barrier 1)
     if (tid == 0) {
+        sFlag[1] = 0;  // tokens flagged by gram_cancels
 #pragma unroll
         for (int b = 0; b < 4; ++b) mbar_init(&bars[b], 1);
         fence_mbar_init();
@@ -364,8 +371,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
 
     // ---- 3. every CTA's records are in
     __syncthreads();
-    const bool ok = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 16), (unsigned long long)nc);
-    if (tid == 0) sFlag[0] = ok ? 1 : 0;
+    if (tid == 0) sFlag[0] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 16), (unsigned int)nc) ? 1 : 0;
     __syncthreads();
     if (!sFlag[0]) {
         if (tid == 0) atomicOr(ctrl, 1u);
@@ -449,10 +455,54 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         *reinterpret_cast<float4 *>(sSt + t * 8) = make_float4(pre[0], pre[1], pre[2], pre[3]);
         sSt[t * 8 + 4] = rstd;
         sSt[t * 8 + 5] = r;
+        const bool fix = gram_cancels(sx, pre, G);
+        sSt[t * 8 + 6] = fix ? 1.f : 0.f;
+        if (fix) atomicAdd(&sFlag[1], 1);
         if (split && c == 0) *reinterpret_cast<float4 *>(pre_out + (size_t)t * 4) = make_float4(pre[0], pre[1], pre[2], pre[3]);
     }
     wsync();
     if (owner_cta) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums and stats -> owner warp
+
+    // ---- 4b. tokens whose streams cancel in X (gram_cancels): sum_h X^2 summed directly.  Every
+    // CTA flags the same tokens (it holds the same sums), so all of them take this branch or
+    // none does.  Each CTA's share over its slice goes to the workspace (one warp per token:
+    // lane v takes vector v, then an xor tree), a second grid barrier, then every CTA adds the
+    // shares in one fixed order and replaces the token's rstd.
+    if (sFlag[1] > 0) {
+        float *fixrec = part + (size_t)T * nc * (kHead + kTail);  // [T][nc]
+        for (int t = wt >> 5; t < T; t += nwork >> 5) {
+            if (sSt[t * 8 + 6] == 0.f) continue;
+            const float4 p4 = *reinterpret_cast<const float4 *>(sSt + t * 8);
+            const float pre[kHC] = {p4.x, p4.y, p4.z, p4.w};
+            float a = 0.f;
+            for (int v = lane; v < nvec && v * kVec < hv; v += 32) {
+                float rf[kHC][8], x[8];
+#pragma unroll
+                for (int j = 0; j < kHC; ++j)
+                    unpack8(*reinterpret_cast<const uint4 *>(sRp + (size_t)t * RS + j * Hs + v * kVec), rf[j]);
+                combine_vec8_x2(rf, pre, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a = fmaf(x[e], x[e], a);
+            }
+            a = warp_sum(a);
+            if (lane == 0) fixrec[(size_t)t * nc + c] = a;
+        }
+        wsync();
+        if (wt == 0) sFlag[2] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 18), (unsigned int)nc) ? 1 : 0;
+        wsync();
+        if (!sFlag[2]) {
+            if (wt == 0) atomicOr(ctrl, 1u);
+            return;
+        }
+        for (int t = wt >> 5; t < T; t += nwork >> 5) {
+            if (sSt[t * 8 + 6] == 0.f) continue;
+            float a = 0.f;
+            for (int q = lane; q < nc; q += 32) a += fixrec[(size_t)t * nc + q];
+            a = warp_sum(a);
+            if (lane == 0) sSt[t * 8 + 4] = 1.f / sqrtf(fmaxf(a, 0.f) / (float)H + sc.rmsnorm_eps);
+        }
+        wsync();
+    }
 
     // ---- 5. combine + RMSNorm of the slice.  Warp-uniform loop: with the MXFP8 output, the four
     // lanes 4a .. 4a+3 hold one block of 32 (nvec is then a multiple of 4).
@@ -523,7 +573,7 @@ bool small_supported(int64_t T, int H, int num_sms, bool mx) {
 }
 size_t small_workspace_bytes(int64_t T, int H) {
     if (T < 1 || T > kSmallMaxT) return 0;
-    return (size_t)((H + 63) / 64) * (size_t)T * (kHead + kTail) * sizeof(float);
+    return (size_t)((H + 63) / 64) * (size_t)T * (kHead + kTail + 1) * sizeof(float);
 }
 
 cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream) {

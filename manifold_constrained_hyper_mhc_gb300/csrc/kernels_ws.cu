@@ -86,6 +86,41 @@ constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 static_assert(kNPre >= kNBuf, "a (pre, rstd) slot is reused only after the combine of its last group");
 
+// phi [4H][24] fp32 -> per CTA rank c, k16-step s, m-tile mt, lane: the A
+// fragment (4 x 32 bits, 8 bf16) of mma.m16n8k16 for the matrix
+//   A[r][k] = hi(phi[k][r]) for r < 24, lo(phi[k][r-24]) for 24 <= r < 48,
+// where hi = bf16(x), lo = bf16(x - hi), and the CTA-local k runs over
+// (stream i, hidden h) as k_local = i*Hs + (h - c*Hs); zero where h >= H.
+__global__ void __launch_bounds__(256)
+pack_phi_kernel(const float *__restrict__ phi, int H, int C, int Hs, uint4 *__restrict__ out) {
+    // a kernel launched after this one with programmatic stream serialization may start now;
+    // it waits for this grid's results before reading them
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int S = kHC * Hs / 16;
+    const int64_t total = (int64_t)C * S * 3 * 32;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= total) return;
+    const int lane = (int)(idx & 31);
+    const int mt = (int)((idx >> 5) % 3);
+    const int s = (int)((idx / 96) % S);
+    const int c = (int)(idx / (96 * (int64_t)S));
+    const int gid = lane >> 2, tig = lane & 3;
+    auto val = [&](int r, int kl) -> float {
+        const int i = kl / Hs, h = c * Hs + kl % Hs;
+        if (h >= H) return 0.f;
+        const float x = phi[((int64_t)i * H + h) * kNumMix + (r % kNumMix)];
+        const float hi = __bfloat162float(__float2bfloat16_rn(x));
+        return r < kNumMix ? hi : x - hi;
+    };
+    const int r0 = mt * 16 + gid, r1 = r0 + 8, k0 = 16 * s + 2 * tig;
+    uint4 v;
+    v.x = pack2_rn(val(r0, k0), val(r0, k0 + 1));
+    v.y = pack2_rn(val(r1, k0), val(r1, k0 + 1));
+    v.z = pack2_rn(val(r0, k0 + 8), val(r0, k0 + 9));
+    v.w = pack2_rn(val(r1, k0 + 8), val(r1, k0 + 9));
+    out[idx] = v;
+}
+
 __device__ __forceinline__ void bwait(uint64_t *bar, uint32_t parity, bool &dead) {
     mbar_wait_timed(bar, parity, dead, kWaitLimitNs);
 }
@@ -189,6 +224,8 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
           float *__restrict__ pre_out, float *__restrict__ post_out, float *__restrict__ res_out,
           float *__restrict__ zstash, unsigned int *__restrict__ status, MxOut mx) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the redo kernel that follows may be scheduled now (it waits for this grid to complete)
+    asm volatile("griddepcontrol.launch_dependents;");
     // the 128-byte swizzled TMA boxes need a 1024-byte aligned base (1 KB of slack is allocated)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int nHB = Hs / 64;
@@ -209,6 +246,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
 
     const int h0 = c * Hs;
     const int nvec = Hs / kVec;  // <= 56
+    unsigned int *redo_list = reinterpret_cast<unsigned int *>(zstash + T * 16);  // [T]: tokens for redo_kernel
     const int nB16 = Hs / 16;    // 16-wide hidden blocks of the slice, <= 28
     const int64_t ngroups = (T + kG - 1) / kG;
     const int nclusters = gridDim.x / kC;
@@ -670,6 +708,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             }
             if (valid) {
                 const int64_t t = t0 + g;
+                // streams that cancel in X: the combine ran with this rstd; the token goes on the
+                // list whose layer inputs redo_kernel recomputes with a direct sum after this
+                // kernel (checked after the sends, off the path every CTA's combine waits for)
+                if (lane == 0 && gram_cancels(sx, pre, G)) redo_list[atomicAdd(status + kRedoCountWord, 1u)] = (unsigned)t;
                 if (lane < 4) pre_out[t * 4 + lane] = pv;
                 else if (lane < 8)
                     post_out[t * 4 + lane - 4] = sc.hc_post_scale / (1.f + expf(-(a_post * z + bl)));
@@ -754,7 +796,15 @@ size_t ws_pack_bytes(int H) {
     return (size_t)kC * (kHC * Hs / 16) * 96 * 16;
 }
 
-size_t ws_stash_bytes(int64_t T) { return (size_t)T * 16 * 4; }
+cudaError_t launch_ws_pack(const float *phi, int H, uint4 *out, cudaStream_t stream) {
+    const int Hs = ws_slice(H);
+    const int64_t total = (int64_t)kC * (kHC * Hs / 16) * 96;
+    pack_phi_kernel<<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(phi, H, kC, Hs, out);
+    return cudaGetLastError();
+}
+
+// residual-mix logits [T][16] fp32, then the list of tokens for redo_kernel [T] u32
+size_t ws_stash_bytes(int64_t T) { return (size_t)T * 16 * 4 + (size_t)T * 4; }
 
 cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream) {
     if (!ws_supported(a.H)) return cudaErrorInvalidValue;
@@ -813,9 +863,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
             return e;
     }
 
-    const int64_t total = (int64_t)kC * (kHC * Hs / 16) * 96;
-    launch_pack_phi(a.phi, a.H, kC, Hs, a.phi_pack, total, stream);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!a.prepacked && (e = launch_ws_pack(a.phi, a.H, a.phi_pack, stream)) != cudaSuccess) return e;
 
     const bool mxo = a.mx.q != nullptr;
     auto kern = post ? (mxo ? ws_kernel<true, true> : ws_kernel<true, false>)
@@ -859,7 +907,10 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         }
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
-    cfg.numAttrs = 2;
+    // with the packing launch before it, overlap the two (the projection warps wait for the packed
+    // phi); with phi packed by the caller there is nothing to overlap, and the kernel reads its
+    // inputs from its first instruction, so it is launched in plain stream order
+    cfg.numAttrs = a.prepacked ? 1 : 2;
     mark_main_kernel(stream, true);
     e = cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
                            a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);

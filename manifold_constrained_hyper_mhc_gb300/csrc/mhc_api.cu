@@ -94,39 +94,10 @@ mhc_status current_device(Device &d) {
     return MHC_OK;
 }
 
-// Cluster schedule geometries: cluster size C, tokens per group G, and the
-// shared-memory budget per CTA (one or two CTAs per SM).
-struct ClusterGeom {
-    int C, G;
-    size_t smem_limit;
-};
-constexpr size_t kMaxDynSmem = 227 * 1024;
-constexpr ClusterGeom kGeom8x16{8, 16, kMaxDynSmem};
-constexpr ClusterGeom kGeom8x8{8, 8, kMaxDynSmem / 2 - 1024};
-constexpr ClusterGeom kGeomDefault = kGeom8x8;
-
-const ClusterGeom *geom_of(int sched) {
-    switch (sched) {
-        case MHC_SCHEDULE_CLUSTER: return &kGeomDefault;
-        case MHC_SCHEDULE_CLUSTER_8x16: return &kGeom8x16;
-        case MHC_SCHEDULE_CLUSTER_8x8: return &kGeom8x8;
-        default: return nullptr;
-    }
-}
-
-bool cluster_fits(const ClusterGeom &g, int64_t H) {
-    return mhc::fused_smem_bytes((int)H, g.C, g.G) <= g.smem_limit;
-}
-
 size_t workspace_bytes_for(int64_t T, int64_t H) {
     size_t sched = mhc::split_workspace_bytes(T, H);
     if (H >= 8 && H <= MHC_MAX_HIDDEN)
     {
-        for (const ClusterGeom *g : {&kGeom8x16, &kGeom8x8})
-            sched = std::max(sched, mhc::fused_pack_bytes((int)H, g->C));
-        sched = std::max(sched, mhc::fused_tmem_pack_bytes((int)H));
-        sched = std::max(sched, ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe_stash_bytes(T));
-        sched = std::max(sched, ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::pipe2_stash_bytes(T));
         sched = std::max(sched, ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::ws_stash_bytes(T));
         sched = std::max(sched, mhc::small_workspace_bytes(T, (int)H));
         sched = std::max(sched, mhc::bcast_workspace_bytes(T, H));
@@ -141,8 +112,7 @@ constexpr int64_t kSmallAutoMaxT = 32;
 int auto_schedule(int64_t T, int64_t H, int sms, bool mx = false) {
     if (T <= kSmallAutoMaxT && mhc::small_supported(T, (int)H, sms, mx)) return MHC_SCHEDULE_SMALL;
     if (mhc::ws_supported((int)H)) return MHC_SCHEDULE_WS;
-    if (mhc::pipe_supported((int)H)) return MHC_SCHEDULE_PIPE;
-    return cluster_fits(kGeomDefault, H) ? MHC_SCHEDULE_CLUSTER : MHC_SCHEDULE_SPLIT;
+    return MHC_SCHEDULE_SPLIT;
 }
 
 int choose_schedule(int64_t T, int64_t H, int sms, bool mx) {
@@ -166,7 +136,7 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                         float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
                         void *workspace, size_t workspace_bytes, void *stream, bool fused,
                         uint8_t *mx_q = nullptr, uint8_t *mx_scale = nullptr, int mx_mode = 0,
-                        const mhc::SideStream *side = nullptr) {
+                        const mhc::SideStream *side = nullptr, const void *packed_phi = nullptr) {
     mhc_status st;
     g_launches = 0;
     const bool mx = mx_q != nullptr || mx_scale != nullptr;
@@ -191,6 +161,8 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                                    {prev_comb_res_mix, "prev_comb_res_mix"},
                                    {residual_out, "residual_out"}})) != MHC_OK)
         return st;
+    if (packed_phi != nullptr && !aligned16(packed_phi))
+        return fail(MHC_ERR_INVALID_ARG, "packed_phi is not 16-byte aligned");
     if (workspace == nullptr) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(MHC_ERR_WORKSPACE, "workspace is not 256-byte aligned");
@@ -203,7 +175,8 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
         sPP{fused ? prev_post_mix : nullptr, tok * 16}, sPC{fused ? prev_comb_res_mix : nullptr, tok * 64},
         sPhi{phi, (size_t)H * 4 * 24 * 4}, sB{bias, 96}, sMS{mix_scales, 12}, sG{rmsnorm_weight, (size_t)H * 2},
         sW{workspace, need};
-    const Span ins[] = {sR, sY, sPP, sPC, sPhi, sB, sMS, sG};
+    const Span sPk{packed_phi, packed_phi != nullptr ? mhc::ws_pack_bytes((int)H) : 0};
+    const Span ins[] = {sR, sY, sPP, sPC, sPhi, sB, sMS, sG, sPk};
     const Span oRo{fused ? residual_out : nullptr, tok * 4 * H * 2}, oX{layer_in_out, tok * H * 2},
         oPre{pre_mix_out, tok * 16}, oPost{post_mix_out, tok * 16}, oRes{comb_res_mix_out, tok * 64};
     const Span oQ{mx_q, mx ? tok * H : 0}, oS{mx_scale, mx ? mx_scale_bytes(T, H) : 0};
@@ -211,7 +184,7 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
     const char *out_names[] = {"residual_out", "layer_in_out", "pre_mix_out", "post_mix_out",
                                "comb_res_mix_out", "workspace", "layer_in_fp8", "layer_in_scales"};
     for (int o = 0; o < 8; ++o) {
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 9; ++i) {
             if (o == 0 && i == 0 && residual_out == residual) continue;  // in-place residual update
             if (overlap(outs[o], ins[i]))
                 return fail(MHC_ERR_INVALID_ARG, "%s overlaps an input", out_names[o]);
@@ -246,62 +219,6 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             g_launches = 3;
             break;
         }
-        case MHC_SCHEDULE_CLUSTER:
-        case MHC_SCHEDULE_CLUSTER_8x16:
-        case MHC_SCHEDULE_CLUSTER_8x8: {
-            const ClusterGeom &geom = *geom_of(sched);
-            if (!cluster_fits(geom, H))
-                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster schedule's shared memory",
-                            (long long)H);
-            mhc::FusedArgs a{};
-            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
-            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
-            a.T = T; a.H = (int)H; a.s = s;
-            a.R_out = fused ? residual_out : nullptr;
-            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
-            a.res_out = comb_res_mix_out;
-            a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
-            a.C = geom.C; a.G = geom.G;
-            e = mhc::launch_fused(a, cs);
-            g_launches = 2;
-            break;
-        }
-        case MHC_SCHEDULE_PIPE: {
-            if (!mhc::pipe_supported((int)H))
-                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the pipe schedule", (long long)H);
-            mhc::FusedArgs a{};
-            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
-            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
-            a.T = T; a.H = (int)H; a.s = s;
-            a.R_out = fused ? residual_out : nullptr;
-            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
-            a.res_out = comb_res_mix_out;
-            char *ws = static_cast<char *>(workspace) + mhc::kControlBytes;
-            a.phi_pack = reinterpret_cast<uint4 *>(ws);
-            float *zstash = reinterpret_cast<float *>(ws + ((mhc::pipe_pack_bytes((int)H) + 255) & ~size_t(255)));
-            a.C = 16; a.G = 8;
-            e = mhc::launch_pipe(a, static_cast<unsigned int *>(workspace), zstash, cs);
-            g_launches = 2;
-            break;
-        }
-        case MHC_SCHEDULE_PIPE2: {
-            if (!mhc::pipe2_supported((int)H))
-                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the pipe2 schedule", (long long)H);
-            mhc::FusedArgs a{};
-            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
-            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
-            a.T = T; a.H = (int)H; a.s = s;
-            a.R_out = fused ? residual_out : nullptr;
-            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
-            a.res_out = comb_res_mix_out;
-            char *ws = static_cast<char *>(workspace) + mhc::kControlBytes;
-            a.phi_pack = reinterpret_cast<uint4 *>(ws);
-            float *zstash = reinterpret_cast<float *>(ws + ((mhc::pipe2_pack_bytes((int)H) + 255) & ~size_t(255)));
-            a.C = 16; a.G = 8;
-            e = mhc::launch_pipe2(a, static_cast<unsigned int *>(workspace), zstash, cs);
-            g_launches = 2;
-            break;
-        }
         case MHC_SCHEDULE_WS: {
             if (!mhc::ws_supported((int)H))
                 return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the ws schedule", (long long)H);
@@ -313,19 +230,27 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
             a.res_out = comb_res_mix_out;
             char *ws = static_cast<char *>(workspace) + mhc::kControlBytes;
-            a.phi_pack = reinterpret_cast<uint4 *>(ws);
+            a.phi_pack = packed_phi != nullptr ? static_cast<uint4 *>(const_cast<void *>(packed_phi))
+                                               : reinterpret_cast<uint4 *>(ws);
+            a.prepacked = packed_phi != nullptr;
             float *zstash = reinterpret_cast<float *>(ws + ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)));
-            a.C = 16; a.G = 8;
             // with the bf16 layer input wanted as well, a separate streaming quantize pass over it
             // is cheaper than ws's in-kernel epilogue (which lengthens the ring's critical chain);
             // both give the same bits
             const bool mx_pass = mx && layer_in_out != nullptr;
             a.mx = mx_pass ? mhc::MxOut{nullptr, nullptr, 0} : mxo;
             e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
-            g_launches = 2;
+            g_launches = a.prepacked ? 1 : 2;
+            if (e == cudaSuccess) {
+                // tokens whose streams cancel in X, listed by the ws kernel: layer input redone
+                e = mhc::launch_redo(fused ? residual_out : residual, rmsnorm_weight, rmsnorm_eps, T, (int)H,
+                                     pre_mix_out, layer_in_out, a.mx, static_cast<unsigned int *>(workspace),
+                                     reinterpret_cast<const unsigned int *>(zstash + (size_t)T * 16), cs);
+                g_launches += 1;
+            }
             if (e == cudaSuccess && mx_pass) {
                 e = mhc::launch_mx_quantize(layer_in_out, T, (int)H, mxo, dev.sms, cs);
-                g_launches = 3;
+                g_launches += 1;
             }
             break;
         }
@@ -346,22 +271,6 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             e = mhc::launch_small(a, static_cast<unsigned int *>(workspace), dev.sms, cs);
             g_launches = side != nullptr ? 2 : 1;
             side = nullptr;  // done: the tail kernel ran on the side stream
-            break;
-        }
-        case MHC_SCHEDULE_CLUSTER16: {
-            if (!mhc::fused_tmem_supported((int)H))
-                return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the cluster16 schedule", (long long)H);
-            mhc::FusedArgs a{};
-            a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
-            a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
-            a.T = T; a.H = (int)H; a.s = s;
-            a.R_out = fused ? residual_out : nullptr;
-            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
-            a.res_out = comb_res_mix_out;
-            a.phi_pack = reinterpret_cast<uint4 *>(static_cast<char *>(workspace) + mhc::kControlBytes);
-            a.C = 16; a.G = 16;
-            e = mhc::launch_fused_tmem(a, static_cast<unsigned int *>(workspace), cs);
-            g_launches = 2;
             break;
         }
         default:
@@ -640,11 +549,66 @@ mhc_status mhc_post_sqrsum(const mhc_bf16 *residual, const mhc_bf16 *layer_out, 
                        residual_out, sqrsum_out, stream);
 }
 
+size_t mhc_packed_phi_bytes(int64_t H) {
+    if (H < 8 || H > MHC_MAX_HIDDEN || H % 8 != 0) return 0;
+    return mhc::ws_pack_bytes((int)H);
+}
+
+mhc_status mhc_pack_phi(const float *phi, int64_t H, void *packed_phi, size_t packed_bytes, void *stream) {
+    mhc_status st;
+    g_launches = 0;
+    if ((st = check_sizes(1, H)) != MHC_OK) return st;
+    if ((st = check_ptrs({{phi, "phi"}, {packed_phi, "packed_phi"}})) != MHC_OK) return st;
+    const size_t need = mhc::ws_pack_bytes((int)H);
+    if (packed_bytes < need) return fail(MHC_ERR_INVALID_ARG, "packed_phi has %zu bytes, needs %zu", packed_bytes, need);
+    if (overlap({phi, (size_t)H * 4 * 24 * 4}, {packed_phi, need}))
+        return fail(MHC_ERR_INVALID_ARG, "packed_phi overlaps phi");
+    Device dev;
+    if ((st = current_device(dev)) != MHC_OK) return st;
+    cudaError_t e = mhc::launch_ws_pack(phi, (int)H, static_cast<uint4 *>(packed_phi), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches = 1;
+    return MHC_OK;
+}
+
+mhc_status mhc_shifted_post_pre_prepacked(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
+                                          const float *prev_post_mix, const float *prev_comb_res_mix,
+                                          const float *phi, const void *packed_phi, const float *bias,
+                                          const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T,
+                                          int64_t H, float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+                                          float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+                                          mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                                          float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    if (packed_phi == nullptr && T > 0) {
+        g_launches = 0;
+        return fail(MHC_ERR_INVALID_ARG, "packed_phi is NULL");
+    }
+    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                        comb_res_mix_out, workspace, workspace_bytes, stream, true, nullptr, nullptr, 0, nullptr,
+                        packed_phi);
+}
+
+mhc_status mhc_pre_prepacked(const mhc_bf16 *residual, const float *phi, const void *packed_phi, const float *bias,
+                             const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
+                             float hc_norm_eps, float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps,
+                             int sinkhorn_iters, mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
+                             float *comb_res_mix_out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (packed_phi == nullptr && T > 0) {
+        g_launches = 0;
+        return fail(MHC_ERR_INVALID_ARG, "packed_phi is NULL");
+    }
+    return run_post_pre(residual, nullptr, nullptr, nullptr, phi, bias, mix_scales, rmsnorm_weight, T, H,
+                        hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters, nullptr, layer_in_out,
+                        pre_mix_out, post_mix_out, comb_res_mix_out, workspace, workspace_bytes, stream, false,
+                        nullptr, nullptr, 0, nullptr, packed_phi);
+}
+
 mhc_status mhc_set_schedule(int schedule) {
-    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_CLUSTER16 &&
-        schedule != MHC_SCHEDULE_PIPE && schedule != MHC_SCHEDULE_PIPE2 && schedule != MHC_SCHEDULE_WS &&
-        schedule != MHC_SCHEDULE_SMALL && schedule != MHC_SCHEDULE_BCAST &&
-        geom_of(schedule) == nullptr)
+    if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_WS &&
+        schedule != MHC_SCHEDULE_SMALL && schedule != MHC_SCHEDULE_BCAST)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);
     return MHC_OK;

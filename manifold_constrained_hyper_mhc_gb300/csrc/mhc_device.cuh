@@ -330,6 +330,23 @@ __device__ __forceinline__ float heads_and_sinkhorn(float z, const float *bias, 
     return lane < 4 ? p : q;
 }
 
+// ---- step (4): the square sum of X from the Gram matrix --------------------
+// The fused schedules take sum_h X^2 as pre^T G pre, G the Gram matrix of the four bf16
+// streams (G_ij = sum_h R'_i[h] R'_j[h], accumulated in fp32).  Its rounding error is a
+// small multiple k of 2^-24 * sum_ij pre_i pre_j |G_ij| <= (sum_i pre_i sqrt(G_ii))^2
+// <= 4 D, D = sum_i pre_i^2 G_ii (Cauchy-Schwarz twice).  When the streams cancel in X
+// (anti-correlated streams with similar pre weights) pre^T G pre is a small difference of such
+// terms and loses its accuracy; gram_cancels() flags a token whose result is below D / 16, and
+// the schedules then sum X^2 over the combined row directly.  Above the threshold the relative
+// error of the Gram form stays below 64 k 2^-24 (far below a bf16 ulp of the output).
+// Independent streams give pre^T G pre / D ~ 1 (up to O(H^-1/2)), identical ones >= 1.  No
+// square root: the test sits on the latency-bound path of the small schedule.
+constexpr float kGramCancel = 1.f / 16.f;
+__device__ __forceinline__ bool gram_cancels(float sx, const float (&pre)[kHC], const float *G /*diagonal 0..3*/) {
+    const float d = pre[0] * pre[0] * G[0] + pre[1] * pre[1] * G[1] + pre[2] * pre[2] * G[2] + pre[3] * pre[3] * G[3];
+    return sx < kGramCancel * d;
+}
+
 // Deterministic warp sum (fixed xor-tree order).
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -17,6 +17,9 @@ constexpr int kPartStride = 32;  // floats per (token, chunk) record: z[24], squ
 // Bytes at the start of every workspace reserved for the control block
 // (device status word, barrier counters).
 constexpr size_t kControlBytes = 256;
+// 32-bit words of the control block: the length of the redo list (tokens whose streams cancel
+// in X, see redo_kernel) and the count of redo CTAs done; both zero between calls.
+constexpr int kRedoCountWord = 32, kRedoDoneWord = 33;
 
 // A second stream for the off-critical-path part of a split call: `fork` is recorded on the
 // main stream once the records are in, the side stream waits on it, and `join` is recorded on
@@ -49,7 +52,7 @@ inline size_t split_workspace_bytes(int64_t T, int64_t H) {
 
 cudaError_t launch_split(const SplitArgs &a, cudaStream_t stream);
 
-// Cluster schedule (kernels_fused.cu).
+// Arguments of the warp-specialised cluster schedule (kernels_ws.cu).
 struct FusedArgs {
     const uint16_t *R;  // residual (fused) or already post-updated residual (pre only)
     const uint16_t *Y;
@@ -61,52 +64,36 @@ struct FusedArgs {
     uint16_t *R_out;  // nullptr: pre only
     uint16_t *X_out;
     float *pre_out, *post_out, *res_out;
-    uint4 *phi_pack;  // workspace: fused_pack_bytes(H, C)
-    int C, G;         // cluster size, tokens per group
-    MxOut mx;         // MXFP8 layer input (mx.q == nullptr: none); ws and small schedules only
+    uint4 *phi_pack;  // ws_pack_bytes(H): the workspace (packed by the call) or the caller's packed phi
+    bool prepacked;   // phi_pack already holds the packed phi (no packing launch)
+    MxOut mx;         // MXFP8 layer input (mx.q == nullptr: none)
 };
 
-int fused_slice(int H, int C);                     // hidden elements per CTA (multiple of 16)
-size_t fused_pack_bytes(int H, int C);             // packed phi fragments
-size_t fused_smem_bytes(int H, int C, int G);      // dynamic shared memory per CTA
-cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
-// phi [4H][24] fp32 -> mma A fragments for a cluster of C CTAs of slice Hs
-void launch_pack_phi(const float *phi, int H, int C, int Hs, uint4 *out, int64_t total, cudaStream_t stream);
-
-// Cluster-of-16 schedule with phi resident in tensor memory (kernels_fused_tmem.cu).
-int fused_tmem_slice(int H);
-bool fused_tmem_supported(int H);
-size_t fused_tmem_pack_bytes(int H);
-cudaError_t launch_fused_tmem(const FusedArgs &a, unsigned int *status, cudaStream_t stream);
-
-// Pipelined cluster-of-16 schedule (kernels_pipe.cu).
-int pipe_slice(int H);
-bool pipe_supported(int H);
-size_t pipe_pack_bytes(int H);
-size_t pipe_stash_bytes(int64_t T);
-cudaError_t launch_pipe(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
-
-// Pipelined cluster-of-16 schedule with the projection on tcgen05 (kernels_pipe2.cu).
-int pipe2_slice(int H);
-bool pipe2_supported(int H);
-size_t pipe2_pack_bytes(int H);
-size_t pipe2_stash_bytes(int64_t T);
-cudaError_t launch_pipe2(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
 // Warp-specialised pipelined cluster-of-16 schedule (kernels_ws.cu).
 int ws_slice(int H);
 bool ws_supported(int H);
 size_t ws_pack_bytes(int H);
+// phi [4H][24] fp32 -> the packed fragments ws reads (ws_pack_bytes(H) bytes at out).
+cudaError_t launch_ws_pack(const float *phi, int H, uint4 *out, cudaStream_t stream);
 size_t ws_stash_bytes(int64_t T);
 cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
 
 // Small-T schedule (kernels_small.cu): one cooperative launch, one CTA per hidden slice,
-// one grid barrier on a 64-bit arrival counter at control-block bytes 64..71.
+// grid barriers on 64-bit words at control-block bytes 64..71 (after the partial sums) and
+// 72..79 (the direct square sums of tokens whose streams cancel in X, when there are any).
 constexpr int kSmallMaxT = 128;
 int small_ctas(int H, int num_sms);
 int small_slice(int H, int num_sms, int align);  // align 8, or 32 for the MXFP8 output
 bool small_supported(int64_t T, int H, int num_sms, bool mx);
 size_t small_workspace_bytes(int64_t T, int H);  // upper bound over SM counts
 cudaError_t launch_small(const SplitArgs &a, unsigned int *ctrl, int num_sms, cudaStream_t stream);
+
+// After the ws kernel on the same stream: the layer input (and its MXFP8 form, mx.q != nullptr)
+// of the tokens listed in `list` (length in control-block word kRedoCountWord), with sum_h X^2
+// summed directly (kernels_redo.cu).  Rp is the R' the main kernel read or wrote.
+cudaError_t launch_redo(const uint16_t *Rp, const uint16_t *gamma, float rmsnorm_eps, int64_t T, int H,
+                        const float *pre_out, uint16_t *X_out, const MxOut &mx, unsigned int *ctrl,
+                        const unsigned int *list, cudaStream_t stream);
 
 // Records the events set by mhc_set_main_kernel_events (if any) on `stream` right before
 // (start) and after (stop) the launch of a call's main kernel.

@@ -33,8 +33,8 @@ namespace {
 constexpr size_t kScratchBytes = size_t(4) << 20;
 
 // Zero-initialised when the module loads, which is the state the op's
-// workspace contract asks for before first use; every successful call leaves
-// it in a state the next call can use.
+// workspace contract asks for before first use; every call that completes
+// leaves it in a state the next call can use, whatever its T and H.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -67,7 +67,10 @@ extern "C" MHC_API mhc_status mhc_shifted_post_pre_noalloc(
     float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
     mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
     void *stream) {
-    if (T < 0 || H < 0) return MHC_ERR_INVALID_ARG;
+    if (T < 0 || H < 0) {
+        mhc::set_last_error("mhc_shifted_post_pre_noalloc: T and H must not be negative");
+        return MHC_ERR_INVALID_ARG;
+    }
     const size_t need = mhc_workspace_size(T, H);
     if (need > kScratchBytes) {
         char msg[256];
@@ -93,4 +96,20 @@ extern "C" MHC_API mhc_status mhc_shifted_post_pre_noalloc(
                                 hc_post_scale, sinkhorn_eps, sinkhorn_iters, residual_out,
                                 layer_in_out, pre_mix_out, post_mix_out, comb_res_mix_out, scratch,
                                 kScratchBytes, stream);
+}
+
+// The static scratch holds a control block like any workspace: a status word that a
+// bounded device-side wait sets when it gives up, and the grid barrier's word.  Callers of
+// the allocation-free entry point never see the array's address, so this reads (and, after
+// a timeout, clears) that block for them, as mhc_check_status does for a workspace.
+extern "C" MHC_API mhc_status mhc_noalloc_check_status(void *stream) {
+    void *scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) {
+        char msg[256];
+        std::snprintf(msg, sizeof msg, "mhc_noalloc_check_status: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        mhc::set_last_error(msg);
+        return MHC_ERR_CUDA;
+    }
+    return mhc_check_status(scratch, stream);
 }

@@ -28,7 +28,6 @@ its own (sampled parity checks at full size need this).
 from __future__ import annotations
 
 import concurrent.futures as cf
-import itertools
 import os
 from dataclasses import dataclass, field
 
@@ -91,24 +90,20 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-_PERMS = np.array(
-    [[[1.0 if p[a] == c else 0.0 for c in range(HC)] for a in range(HC)]
-     for p in itertools.permutations(range(HC))],
-    dtype=np.float64,
-)  # [24, 4, 4] permutation matrices
+# The previous layer's residual mixes: 1024 seeded matrices, each the 20-iteration Sinkhorn
+# normalisation of exp(N(0, 0.5)) as the workload definition states, written once by
+# tests/golden/make_prev_comb_table.py (with the CPU oracle's Sinkhorn, so that no arithmetic of
+# the op lives here); every token takes one of them by a seeded index.
+_PREV_COMB_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tests", "golden",
+                               "prev_comb_sinkhorn20.npy")
+_prev_comb_table = None
 
 
-def _doubly_stochastic(rng: np.random.Generator, n: int) -> np.ndarray:
-    """n random 4x4 doubly stochastic matrices with positive entries.
-
-    Drawn as convex combinations of the 24 permutation matrices with
-    log-normal weights (Birkhoff-von Neumann sampling).  Row and column sums are
-    1 up to rounding.  This stands in for "a previous layer's Sinkhorn output"
-    without running any Sinkhorn iteration here.
-    """
-    w = rng.lognormal(0.0, 1.0, size=(n, len(_PERMS)))
-    w /= w.sum(axis=1, keepdims=True)
-    return np.einsum("np,pac->nac", w, _PERMS).astype(np.float32)
+def prev_comb_table() -> np.ndarray:
+    global _prev_comb_table
+    if _prev_comb_table is None:
+        _prev_comb_table = np.load(_PREV_COMB_PATH)
+    return _prev_comb_table
 
 
 def weights(w: Workload):
@@ -130,7 +125,7 @@ def _block(w: Workload, b: int):
     Y = rng.standard_normal((n, w.H), dtype=np.float32)
     # prev post mix: 2 * logistic(N(0,1)), i.e. a scaled logit-normal draw
     prev_post = (2.0 / (1.0 + np.exp(-rng.standard_normal((n, HC))))).astype(np.float32)
-    prev_comb = _doubly_stochastic(rng, n)
+    prev_comb = prev_comb_table()[rng.integers(0, len(prev_comb_table()), size=n)]
     if w.token_scale:
         s = (10.0 ** rng.uniform(-2.0, 2.0, size=n)).astype(np.float32)
         R *= s[:, None, None]
@@ -165,6 +160,55 @@ def tokens(w: Workload, t0: int = 0, t1: int | None = None):
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(blocks), os.cpu_count() or 1))) as ex:
         list(ex.map(fill, blocks))
     return R, Y, post, comb
+
+
+CANCEL_KINDS = ("exact", "mild", "severe", "partial", "independent")
+
+
+def cancellation_case(T: int, H: int, seed: int):
+    """Inputs whose streams cancel in the combined row X = sum_i pre_i R'_i (an adversarial case
+    for any shortcut that forms sum_h X^2 from per-stream sums).
+
+    The previous mixes are the identity residual mix and a zero post mix, so R' = R exactly.
+    phi's logit columns 1 and 3 repeat columns 0 and 2, and the matching biases repeat too,
+    so pre_1 = pre_0 and pre_3 = pre_2 whatever the streams are.  Token t of kind
+    CANCEL_KINDS[t % 5], with A, B ~ N(0,1) * 10**U(0, 2) per token and d ~ N(0, s^2):
+      exact       R = [A, -A, B, -B]                 (X is zero up to rounding)
+      mild        R = [A, -A + d, B, -B + d'], s = 2^-6 |scale|
+      severe      R = [A, -A + d, B, -B + d'], s = 2^-10 |scale|
+      partial     R = [A, -A + d, B, C],       s = 2^-10 |scale|, C ~ N(0,1) * scale
+      independent R = [A, B, C, D]
+    Returns (R, Y, prev_post, prev_comb, phi, bias, mix_scales, gamma) like tokens() and
+    weights()."""
+    rng = np.random.default_rng([seed, 7])
+    phi = rng.standard_normal((HC * H, NMIX), dtype=np.float32) * np.float32(0.02)
+    phi[:, 1] = phi[:, 0]
+    phi[:, 3] = phi[:, 2]
+    bias = rng.standard_normal(NMIX, dtype=np.float32) * np.float32(0.1)
+    bias[1] = bias[0]
+    bias[3] = bias[2]
+    gamma = f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(H, dtype=np.float32))
+    mix_scales = np.array(MIX_SCALES, dtype=np.float32)
+    scale = (10.0 ** rng.uniform(0.0, 2.0, size=T)).astype(np.float32)
+    Z = rng.standard_normal((T, HC, H), dtype=np.float32) * scale[:, None, None]
+    D = rng.standard_normal((T, 2, H), dtype=np.float32) * scale[:, None, None]
+    R = Z.copy()
+    kind = np.arange(T) % len(CANCEL_KINDS)
+    for k, name in enumerate(CANCEL_KINDS):
+        m = kind == k
+        if name == "exact":
+            R[m, 1] = -Z[m, 0]
+            R[m, 3] = -Z[m, 2]
+        elif name in ("mild", "severe"):
+            s_ = np.float32(2.0 ** -6 if name == "mild" else 2.0 ** -10)
+            R[m, 1] = -Z[m, 0] + s_ * D[m, 0]
+            R[m, 3] = -Z[m, 2] + s_ * D[m, 1]
+        elif name == "partial":
+            R[m, 1] = -Z[m, 0] + np.float32(2.0 ** -10) * D[m, 0]
+    Y = f32_to_bf16_bits(rng.standard_normal((T, H), dtype=np.float32))
+    prev_post = np.zeros((T, HC), np.float32)
+    prev_comb = np.broadcast_to(np.eye(HC, dtype=np.float32), (T, HC, HC)).copy()
+    return f32_to_bf16_bits(R), Y, prev_post, prev_comb, phi, bias, mix_scales, gamma
 
 
 def scalars():

@@ -124,3 +124,48 @@ def test_bench_byte_counts_match_the_scope_table():
     assert abs(bench.algorithmic_bytes(6, 7168) / 1e6 - 3.63) < 0.005
     assert abs(bench.algorithmic_bytes(8192, 7168) / 1e9 - 1.1786) < 0.0001
     assert bench.algorithmic_bytes(8192, 7168, True) - bench.algorithmic_bytes(8192, 7168) == 8192 * (7168 + 224)
+
+
+def test_removed_schedule_ids_are_refused(mhc_lib):
+    """Ids 2-7 named the cluster and pipelined schedules that ws superseded; they are gone."""
+    L = mhc_lib.lib()
+    for sid in range(2, 8):
+        assert L.mhc_set_schedule(sid) == -1
+    for sid in (0, 1, 8, 9, 10):
+        assert L.mhc_set_schedule(sid) == 0
+    assert L.mhc_set_schedule(0) == 0
+
+
+def test_noalloc_negative_sizes_are_refused_with_a_message(mhc_lib):
+    L = mhc_lib.lib()
+    P_, I64, F_, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    L.mhc_shifted_post_pre_noalloc.argtypes = [P_] * 8 + [I64, I64, F_, F_, F_, F_, I] + [P_] * 6
+    L.mhc_shifted_post_pre_noalloc.restype = I
+    p = ins(8)
+    outs = ins(5, 0x200000000000)
+    assert L.mhc_set_schedule(999) == -1  # leaves an unrelated message behind
+    for T, H in ((-1, 1024), (4, -8)):
+        assert L.mhc_shifted_post_pre_noalloc(*p, T, H, *SC[:4], SC[4], *outs, None) == -1
+        assert b"must not be negative" in L.mhc_last_error()
+
+
+def test_pack_phi_argument_checks_and_size(mhc_lib):
+    """mhc_packed_phi_bytes: 16 CTA slices of ceil(H / 1024) * 64 hidden values, each 4 * slice / 16
+    k16 steps of three 512-byte fragment tiles (hi and lo bf16 of phi^T); bad calls are refused
+    before any device work."""
+    L = mhc_lib.lib()
+    Z, I64 = ctypes.c_size_t, ctypes.c_int64
+    L.mhc_packed_phi_bytes.argtypes = [I64]
+    L.mhc_packed_phi_bytes.restype = Z
+    L.mhc_pack_phi.argtypes = [ctypes.c_void_p, I64, ctypes.c_void_p, Z, ctypes.c_void_p]
+    for H in (1024, 4096, 7168, 2056):
+        hs = (H + 1023) // 1024 * 64
+        assert L.mhc_packed_phi_bytes(H) == 16 * (4 * hs // 16) * 3 * 512
+    assert L.mhc_packed_phi_bytes(1020) == 0 and L.mhc_packed_phi_bytes(0) == 0
+    phi, out = P(0x100000000), P(0x200000000000)
+    n = L.mhc_packed_phi_bytes(7168)
+    assert L.mhc_pack_phi(phi, 7168, out, n - 16, None) == -1       # too small
+    assert L.mhc_pack_phi(None, 7168, out, n, None) == -1            # no phi
+    assert L.mhc_pack_phi(phi, 7168, None, n, None) == -1            # no output
+    assert L.mhc_pack_phi(phi, 7168, P(0x100000010), n, None) == -1  # overlaps phi
+    assert L.mhc_pack_phi(phi, 1020, out, n, None) == -1             # H % 8

@@ -6,7 +6,7 @@ import pytest
 import oracle
 from manifold_constrained_hyper_mhc_gb300 import synth
 
-from _helpers import F, MIX_ATOL, bf16_check, compare_fused
+from _helpers import F, MIX_ATOL, bf16_check, compare_fused, write_report
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -65,7 +65,7 @@ def check_workload(mhc, w, schedule="auto"):
     assert not msgs, "\n".join(msgs)
 
 
-ALL_SCHEDULES = ["auto", "split", "cluster_8x16", "cluster_8x8", "cluster16", "pipe", "pipe2", "ws", "small"]
+ALL_SCHEDULES = ["auto", "split", "ws", "small"]
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_verify", "mid_batch"])
@@ -80,45 +80,36 @@ def test_ragged_shapes(mhc, T, H, schedule):
     check_workload(mhc, synth.Workload(f"ragged_{T}x{H}", T, H, 100 + T, token_scale=True), schedule)
 
 
-def test_prefill_chunk_full_parity(mhc):
-    """T=8192, H=7168, the bench's workload and launch configuration: every token
-    against the oracle (compared in token chunks to bound host memory)."""
-    w = synth.WORKLOADS["prefill_chunk"]
+def _full_parity(mhc, w, step=1024):
+    """Every token of workload w against the oracle (compared in token chunks to bound host
+    memory).  Returns the GPU outputs (on the device) and the parity report."""
     (phi, bias, ms, gamma), wd = weights_dev(w)
     R, Y, pp, pc = synth.tokens(w)
     o = mhc.shifted_post_pre(dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC)
     torch.cuda.synchronize()
-    msgs = []
-    step = 1024
+    msgs, report = [], {}
     for t0 in range(0, w.T, step):
         s = slice(t0, t0 + step)
         got = {k: (host_bf16(v[s]) if v.dtype == torch.bfloat16 else host(v[s])) for k, v in o.items()}
         ref = oracle.shifted_post_pre(R[s], Y[s], pp[s], pc[s], phi, bias, ms, gamma, **SC, debug=True)
-        msgs += compare_fused(got, ref, (R[s], Y[s], pp[s], pc[s]), gamma, label=f"tokens {t0}+")
-    assert not msgs, "\n".join(msgs)
+        msgs += compare_fused(got, ref, (R[s], Y[s], pp[s], pc[s]), gamma, label=f"tokens {t0}+", report=report)
+    write_report(w.name, report)
+    assert not msgs, "\n".join(msgs[:20])
+    return o, gamma, report
+
+
+def test_prefill_chunk_full_parity(mhc):
+    """T=8192, H=7168, the bench's workload and launch configuration: every token
+    against the oracle."""
+    _full_parity(mhc, synth.WORKLOADS["prefill_chunk"])
 
 
 @pytest.mark.slow
-def test_long_prefill_sampled_parity_and_invariants(mhc):
-    """T=65536, H=7168 with 1% zero-Y and 1% identical-stream tokens: every
-    special token plus a random sample against the oracle; properties that hold
-    at any size on every token."""
+def test_long_prefill_full_parity_and_invariants(mhc):
+    """T=65536, H=7168 with 1% zero-Y and 1% identical-stream tokens: every token against
+    the oracle, and properties that hold at any size on every token."""
     w = synth.WORKLOADS["long_prefill"]
-    (phi, bias, ms, gamma), wd = weights_dev(w)
-    R, Y, pp, pc = synth.tokens(w)
-    o = mhc.shifted_post_pre(dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC)
-    torch.cuda.synchronize()
-    t = np.arange(w.T)
-    rng = np.random.default_rng(99)
-    sample = np.unique(np.concatenate([t[t % 100 == 0], t[t % 100 == 50], rng.choice(w.T, 2048, replace=False),
-                                       np.arange(w.T - 64, w.T)]))
-    idx = torch.from_numpy(sample).cuda()
-    got = {k: (host_bf16(v[idx]) if v.dtype == torch.bfloat16 else host(v[idx])) for k, v in o.items()}
-    ins = (R[sample], Y[sample], pp[sample], pc[sample])
-    ref = oracle.shifted_post_pre(*ins, phi, bias, ms, gamma, **SC, debug=True)
-    msgs = compare_fused(got, ref, ins, gamma, label="long_prefill sample")
-    assert not msgs, "\n".join(msgs)
-    # invariants on all tokens
+    o, gamma, _ = _full_parity(mhc, w, step=2048)
     res = o["comb_res_mix"]
     cs, rs = res.sum(1), res.sum(2)
     eps = SC["sinkhorn_eps"]
@@ -319,3 +310,27 @@ def test_small_schedule_barrier_timeout_is_reported(mhc):
     ref = oracle.shifted_post_pre(R, Y, pp, pc, phi, bias, ms, gamma, **SC, debug=True)
     msgs = compare_fused(got, ref, (R, Y, pp, pc), gamma, label="after timeout")
     assert not msgs, "\n".join(msgs)
+
+
+def test_small_schedule_one_workspace_across_hidden_sizes(mhc):
+    """The small schedule's CTA count follows H (112 CTAs at H = 7168, 64 at 4096, 16 at 1024)
+    and its grid barrier keeps its word in the workspace's control block: calls with those
+    sizes and the first again, in a row on one workspace, each against the oracle, with the
+    status word checked after each."""
+    cases = [synth.Workload("seq_7168", 6, 7168, 61), synth.Workload("seq_4096", 17, 4096, 62),
+             synth.Workload("seq_1024", 32, 1024, 63), synth.Workload("seq_7168b", 5, 7168, 64)]
+    ws = mhc.new_workspace(max(w.T for w in cases), 7168)
+    assert ws.numel() >= max(mhc.workspace_size(w.T, w.H) for w in cases)
+    mhc.set_schedule("small")
+    try:
+        for w in cases:
+            (phi, bias, ms, gamma), wd = weights_dev(w)
+            R, Y, pp, pc = synth.tokens(w)
+            o = mhc.shifted_post_pre(dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC, workspace=ws)
+            mhc.check_status(ws)
+            got = {k: (host_bf16(v) if v.dtype == torch.bfloat16 else host(v)) for k, v in o.items()}
+            ref = oracle.shifted_post_pre(R, Y, pp, pc, phi, bias, ms, gamma, **SC, debug=True)
+            msgs = compare_fused(got, ref, (R, Y, pp, pc), gamma, label=w.name)
+            assert not msgs, "\n".join(msgs)
+    finally:
+        mhc.set_schedule("auto")

@@ -5,8 +5,9 @@ synchronise).  Its scratch is a fixed static array inside the library, so the
 caller passes only inputs and outputs.
 
 Called here through the C ABI (ctypes) and checked against the regular
-mhc_shifted_post_pre on two calls in a row with different inputs, with the
-tolerances of the parity tests.  This file is collected last on purpose.
+mhc_shifted_post_pre on calls in a row with different inputs and sizes, with
+the tolerances of the parity tests; mhc_noalloc_check_status reads the static
+scratch's status word after each.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -31,6 +32,8 @@ def lib(mhc_lib):
     L.mhc_shifted_post_pre_noalloc.argtypes = [P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
                                                P, P, P, P, P, P]
     L.mhc_shifted_post_pre_noalloc.restype = I
+    L.mhc_noalloc_check_status.argtypes = [P]
+    L.mhc_noalloc_check_status.restype = I
     return L
 
 
@@ -67,6 +70,7 @@ def test_noalloc_matches_fused_on_two_calls_in_a_row(lib, mhc_lib):
     got = [_outs(w.T, w.H) for w in cases]
     for w, i, o in zip(cases, ins, got):          # two no-alloc calls back to back
         assert _noalloc(lib, i, w.T, w.H, o) == 0, lib.mhc_last_error().decode()
+    assert lib.mhc_noalloc_check_status(_stream()) == 0, lib.mhc_last_error().decode()
     want = [mhc_lib.shifted_post_pre(*i, **SC) for i in ins]
     torch.cuda.synchronize()
     for w, g, r in zip(cases, got, want):
@@ -75,6 +79,32 @@ def test_noalloc_matches_fused_on_two_calls_in_a_row(lib, mhc_lib):
             assert nbad == 0, f"{w.name} {k}: {nbad} elements beyond tolerance (max {max_ulp} ulp)"
         for k in ("pre_mix", "post_mix", "comb_res_mix"):
             assert float((g[k] - r[k]).abs().max()) <= MIX_ATOL, (w.name, k)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_calls_of_different_hidden_sizes_in_a_row(lib, mhc_lib):
+    """Calls of at most 32 tokens run on the small schedule, whose CTA count follows H (112 at
+    H = 7168, 64 at 4096, 16 at 1024) and whose grid barrier keeps its word in the shared static
+    scratch.  H = 7168, 4096, 1024 and 7168 again in a row: each against mhc_shifted_post_pre
+    on a fresh workspace, and the scratch's status word clear after each."""
+    cases = [synth.Workload("na_7168", 6, 7168, 61), synth.Workload("na_4096", 17, 4096, 62),
+             synth.Workload("na_1024", 32, 1024, 63), synth.Workload("na_7168b", 5, 7168, 64)]
+    for w in cases:
+        assert mhc_lib.auto_schedule(w.T, w.H) == mhc_lib.SCHEDULES["small"]
+        ins = _inputs(w)
+        o = _outs(w.T, w.H)
+        assert _noalloc(lib, ins, w.T, w.H, o) == 0, lib.mhc_last_error().decode()
+        assert lib.mhc_noalloc_check_status(_stream()) == 0, lib.mhc_last_error().decode()
+        r = mhc_lib.shifted_post_pre(*ins, **SC)
+        torch.cuda.synchronize()
+        for k in ("residual_out", "layer_in"):
+            nbad, max_ulp, _ = bf16_check(_bits(o[k]), _bits(r[k]), 0.0)
+            assert nbad == 0, f"{w.name} {k}: {nbad} elements beyond tolerance (max {max_ulp} ulp)"
+        for k in ("pre_mix", "post_mix", "comb_res_mix"):
+            assert float((o[k] - r[k]).abs().max()) <= MIX_ATOL, (w.name, k)
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(lib):
