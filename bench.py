@@ -573,7 +573,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "ws", "small", "bcast"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "ws", "small", "bcast", "tile"])
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--op", default="fused",
                     choices=["fused", "split", "post", "post_sqrsum", "post_int8", "pre", "pre_broadcast"],

@@ -107,9 +107,15 @@ typedef enum mhc_schedule {
                                      T <= 96): one cooperative launch, one CTA per hidden slice
                                      on up to every SM, one bounded grid barrier between the partial
                                      sums and the combine (latency-bound decode calls) */
-    MHC_SCHEDULE_BCAST = 10       /* mhc_pre_broadcast only (H % 64 == 0): one persistent kernel that
+    MHC_SCHEDULE_BCAST = 10,      /* mhc_pre_broadcast only (H % 64 == 0): one persistent kernel that
                                      works from x alone, 8 tokens per tile, x read twice (the second
                                      time from L2); the other calls choose as AUTO */
+    MHC_SCHEDULE_TILE = 11        /* H % 64 == 0, no MXFP8 output: one CTA per SM on tiles of 16 tokens,
+                                     no clusters; a tile's row walked twice in chunks (post, R' to HBM
+                                     and kept in L2, projection with phi read from L2; then the
+                                     combine from R' read back).  AUTO runs it beside ws on the SMs
+                                     that ws's clusters leave idle, on a share of the tokens, for
+                                     calls of at least 2048 tokens; forced, it takes every SM */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */
@@ -192,11 +198,12 @@ MHC_API size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H);
  *                     GEMMs); padding bytes (m >= T, k >= H/32) are not written
  *   scale_mode        MHC_MX_SCALE_FLOOR or MHC_MX_SCALE_CEIL; E is clamped to [-127, 127],
  *                     and an all-zero block gets E = -127
- * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  Runs on the ws and small schedules
- * (AUTO picks one of them); a forced other schedule returns MHC_ERR_UNSUPPORTED.  On ws with
- * layer_in_out given, the quantize is a second streaming pass over the bf16 layer input (the
- * same bits; cheaper there than the in-kernel epilogue).  The bf16
- * output and the mixes are bit-identical to mhc_shifted_post_pre's on the same schedule. */
+ * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  Runs on the ws (with the tile kernel
+ * beside it, as AUTO splits a plain call), tile and small schedules; a forced split schedule
+ * returns MHC_ERR_UNSUPPORTED.  On ws with layer_in_out given, the quantize is a second
+ * streaming pass over the bf16 layer input (the same bits; cheaper there than the in-kernel
+ * epilogue).  The bf16 output and the mixes are bit-identical to mhc_shifted_post_pre's with the
+ * same schedule setting. */
 MHC_API mhc_status mhc_shifted_post_pre_mxfp8(
     const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
     const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,

@@ -27,7 +27,7 @@ MX_SCALE_FLOOR, MX_SCALE_CEIL = 0, 1
 OK = 0
 STATUS = {0: "MHC_OK", -1: "MHC_ERR_INVALID_ARG", -2: "MHC_ERR_UNSUPPORTED", -3: "MHC_ERR_WORKSPACE",
           -4: "MHC_ERR_CUDA", -5: "MHC_ERR_DEVICE_TIMEOUT"}
-SCHEDULES = {"auto": 0, "split": 1, "ws": 8, "small": 9, "bcast": 10}
+SCHEDULES = {"auto": 0, "split": 1, "ws": 8, "small": 9, "bcast": 10, "tile": 11}
 
 
 class MhcError(RuntimeError):

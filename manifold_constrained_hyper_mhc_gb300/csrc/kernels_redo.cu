@@ -23,20 +23,22 @@ namespace mhc {
 
 namespace {
 
-constexpr int kRT = 256;        // threads per CTA
+// One warp per CTA: small enough to be resident beside the main kernel (a ws CTA leaves 4096
+// registers of its SM free), so the grid is in place, waiting, when the main kernel ends.
+constexpr int kRT = 32;            // threads per CTA
 constexpr int64_t kRedoCtas = 32;  // CTAs of the grid (grid-stride over the listed tokens)
 
-__global__ void __launch_bounds__(kRT)
-redo_kernel(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma, float rmsnorm_eps, int H,
+__global__ void __launch_bounds__(kRT, 1)
+redo_kernel(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma, float rmsnorm_eps, int64_t T, int H,
             const float *__restrict__ pre_out, uint16_t *__restrict__ X_out, MxOut mx, unsigned int *ctrl,
             const unsigned int *__restrict__ list) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the main kernel is complete, its writes visible
     // what follows on the stream may launch now; it waits for this grid before it reads
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ float sRed[kRT / 32];
-    __shared__ float sRstd;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const unsigned int n = *reinterpret_cast<volatile unsigned int *>(ctrl + kRedoCountWord);
+    const int tid = threadIdx.x;
+    // (a list longer than the call's tokens can only be left over from an aborted call)
+    const unsigned int n0 = *reinterpret_cast<volatile unsigned int *>(ctrl + kRedoCountWord);
+    const unsigned int n = n0 < (unsigned int)T ? n0 : (unsigned int)T;
     const int nb32 = (H + 31) / 32;  // blocks of 32 values: block b holds vectors 4b .. 4b+3
     const float inv_h = 1.f / (float)H;
     for (unsigned int i = blockIdx.x; i < n; i += gridDim.x) {
@@ -51,7 +53,7 @@ redo_kernel(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma,
             for (int j = 0; j < kHC; ++j) unpack8(ld_ro(row + (int64_t)j * H + v * kVec), rf[j]);
             combine_vec8_x2(rf, pre, x);
         };
-        // sum_h X^2: each thread its blocks in order, then an xor tree, then the warps in order
+        // sum_h X^2: each lane its blocks in order, then an xor tree
         float a = 0.f;
         for (int b = tid; b < nb32; b += kRT) {
 #pragma unroll
@@ -66,15 +68,7 @@ redo_kernel(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma,
             }
         }
         a = warp_sum(a);
-        if (lane == 0) sRed[warp] = a;
-        __syncthreads();
-        if (tid == 0) {
-            float s = 0.f;
-            for (int w = 0; w < kRT / 32; ++w) s += sRed[w];
-            sRstd = __frsqrt_rn(fmaxf(s, 0.f) * inv_h + rmsnorm_eps);
-        }
-        __syncthreads();
-        const float rstd = sRstd;
+        const float rstd = __frsqrt_rn(fmaxf(a, 0.f) * inv_h + rmsnorm_eps);
         for (int b = tid; b < nb32; b += kRT) {
             uint4 ob[4];
 #pragma unroll
@@ -93,11 +87,10 @@ redo_kernel(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma,
                 mx_quantize_block(ob, jj, mx.mode, mx.q + t * (int64_t)H + 32 * b, mx.scale + mx_scale_offset(t, b, H));
             }
         }
-        __syncthreads();  // sRed and sRstd are reused by the next token
     }
-    if (n == 0) return;  // nothing listed: the list is already empty for the next call
+    if (n0 == 0) return;  // nothing listed: the list is already empty for the next call
     // the last CTA to get here clears the list for the next call
-    __syncthreads();
+    __syncwarp();
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(ctrl + kRedoDoneWord, 1u) == gridDim.x - 1) {
@@ -124,7 +117,7 @@ cudaError_t launch_redo(const uint16_t *Rp, const uint16_t *gamma, float rmsnorm
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, redo_kernel, Rp, gamma, rmsnorm_eps, H, pre_out, X_out, mx, ctrl, list);
+    return cudaLaunchKernelEx(&cfg, redo_kernel, Rp, gamma, rmsnorm_eps, T, H, pre_out, X_out, mx, ctrl, list);
 }
 
 }  // namespace mhc

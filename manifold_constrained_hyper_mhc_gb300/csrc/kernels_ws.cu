@@ -222,10 +222,9 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
           const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int64_t T, int H,
           int Hs, RLayout lay, uint16_t *__restrict__ R_out, uint16_t *__restrict__ X_out,
           float *__restrict__ pre_out, float *__restrict__ post_out, float *__restrict__ res_out,
-          float *__restrict__ zstash, unsigned int *__restrict__ status, MxOut mx) {
+          float *__restrict__ zstash, unsigned int *__restrict__ redo_list, int64_t list_len,
+          unsigned int *__restrict__ status, MxOut mx) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // the redo kernel that follows may be scheduled now (it waits for this grid to complete)
-    asm volatile("griddepcontrol.launch_dependents;");
     // the 128-byte swizzled TMA boxes need a 1024-byte aligned base (1 KB of slack is allocated)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int nHB = Hs / 64;
@@ -246,7 +245,6 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
 
     const int h0 = c * Hs;
     const int nvec = Hs / kVec;  // <= 56
-    unsigned int *redo_list = reinterpret_cast<unsigned int *>(zstash + T * 16);  // [T]: tokens for redo_kernel
     const int nB16 = Hs / 16;    // 16-wide hidden blocks of the slice, <= 28
     const int64_t ngroups = (T + kG - 1) / kG;
     const int nclusters = gridDim.x / kC;
@@ -300,6 +298,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         // the kernel may start while the packing launch before it still runs (programmatic
         // dependent launch): wait for its results here, the only place that reads them
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        // the launches after this one (the token-tile kernel on the SMs the clusters leave idle,
+        // the redo pass) may start now: the packed phi they read is complete, and neither waits
+        // for this kernel before its end
+        asm volatile("griddepcontrol.launch_dependents;");
         for (int i = 0; i < nblk(p); ++i) {
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
@@ -711,7 +713,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 // streams that cancel in X: the combine ran with this rstd; the token goes on the
                 // list whose layer inputs redo_kernel recomputes with a direct sum after this
                 // kernel (checked after the sends, off the path every CTA's combine waits for)
-                if (lane == 0 && gram_cancels(sx, pre, G)) redo_list[atomicAdd(status + kRedoCountWord, 1u)] = (unsigned)t;
+                if (lane == 0 && gram_cancels(sx, pre, G)) {
+                    const unsigned int idx = atomicAdd(status + kRedoCountWord, 1u);
+                    if (idx < (unsigned int)list_len) redo_list[idx] = (unsigned int)t;
+                }
                 if (lane < 4) pre_out[t * 4 + lane] = pv;
                 else if (lane < 8)
                     post_out[t * 4 + lane - 4] = sc.hc_post_scale / (1.f + expf(-(a_post * z + bl)));
@@ -805,6 +810,41 @@ cudaError_t launch_ws_pack(const float *phi, int H, uint4 *out, cudaStream_t str
 
 // residual-mix logits [T][16] fp32, then the list of tokens for redo_kernel [T] u32
 size_t ws_stash_bytes(int64_t T) { return (size_t)T * 16 * 4 + (size_t)T * 4; }
+
+cudaError_t ws_resident_ctas(int H, bool post, int &ctas) {
+    const Layout L{ws_slice(H) / 64};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static int cache[64][2];
+    std::lock_guard<std::mutex> lock(g_mu);
+    int &mc = cache[dev][post ? 1 : 0];
+    if (mc == 0) {
+        auto kern = post ? ws_kernel<true, false> : ws_kernel<false, false>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)) != cudaSuccess)
+            return e;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+            return e;
+        cudaLaunchConfig_t q = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kC;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        q.gridDim = dim3(kC);
+        q.blockDim = dim3(kNT);
+        q.dynamicSmemBytes = std::max<size_t>(L.bytes() + 1024, 227 * 1024 / 2 + 1024);
+        q.attrs = attr;
+        q.numAttrs = 1;
+        int n = 0;
+        if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &q)) != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        mc = n;
+    }
+    ctas = mc * kC;
+    return cudaSuccess;
+}
 
 cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream) {
     if (!ws_supported(a.H)) return cudaErrorInvalidValue;
@@ -913,8 +953,9 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     cfg.numAttrs = a.prepacked ? 1 : 2;
     mark_main_kernel(stream, true);
     e = cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
-                           a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, status, a.mx);
-    mark_main_kernel(stream, false);
+                           a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, a.redo_list,
+                           a.redo_len, status, a.mx);
+    if (!a.side_follows) mark_main_kernel(stream, false);  // else after the side kernel
     return e;
 }
 

@@ -122,6 +122,34 @@ int choose_schedule(int64_t T, int64_t H, int sms, bool mx) {
     return auto_schedule(T, H, sms, mx);
 }
 
+int forced_schedule() { return g_forced_schedule.load(std::memory_order_relaxed); }
+
+// The token-tile kernel beside ws: below this many tokens (or with fewer idle SMs) ws runs alone.
+constexpr int64_t kSideMinT = 2048;
+constexpr int kSideMinSms = 8;
+// Measured per-SM rate of the token-tile kernel relative to ws's (prefill chunk, T = 8192,
+// H = 7168, both running together).
+constexpr double kSideRate = 0.55;
+
+// The first token of the token-tile kernel's share (T: ws alone), and in `idle` the SMs ws leaves
+// idle (the tile kernel's grid).  The share follows the two
+// kernels' rates (ws on its resident CTAs, the tile kernel on the idle SMs) and is a whole number
+// of 16-token tiles per idle SM, so the tile kernel's CTAs finish together; ws keeps whole groups
+// of 8 tokens.
+int64_t side_split(int64_t T, int64_t H, bool fused, int sms, int &idle) {
+    idle = 0;
+    if (T < kSideMinT || !mhc::tile_supported(T, H)) return T;
+    int ws_ctas = 0;
+    if (mhc::ws_resident_ctas((int)H, fused, ws_ctas) != cudaSuccess) return T;
+    idle = sms - ws_ctas;
+    if (idle < kSideMinSms) return T;
+    const double f = idle * kSideRate / (ws_ctas + idle * kSideRate);
+    const int64_t per_round = (int64_t)idle * 16;
+    const int64_t rounds = (int64_t)(T * f / per_round + 0.5);
+    if (rounds < 1) return T;
+    return (T - rounds * per_round) / 8 * 8;
+}
+
 size_t mx_scale_bytes(int64_t T, int64_t H) {
     return (size_t)((T + 127) / 128 * 128) * (size_t)((H / 32 + 3) / 4 * 4);
 }
@@ -201,8 +229,8 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
     mhc::Scalars s{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
     const int sched = choose_schedule(T, H, dev.sms, mx);
     const mhc::MxOut mxo{mx_q, mx_scale, mx_mode};
-    if (mx && sched != MHC_SCHEDULE_WS && sched != MHC_SCHEDULE_SMALL)
-        return fail(MHC_ERR_UNSUPPORTED, "the MXFP8 output is produced by the ws and small schedules only");
+    if (mx && sched != MHC_SCHEDULE_WS && sched != MHC_SCHEDULE_SMALL && sched != MHC_SCHEDULE_TILE)
+        return fail(MHC_ERR_UNSUPPORTED, "the MXFP8 output is produced by the ws, tile and small schedules only");
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     switch (sched) {
@@ -219,9 +247,14 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             g_launches = 3;
             break;
         }
-        case MHC_SCHEDULE_WS: {
-            if (!mhc::ws_supported((int)H))
+        case MHC_SCHEDULE_WS:
+        case MHC_SCHEDULE_TILE: {
+            const bool tile_alone = sched == MHC_SCHEDULE_TILE;
+            if (!tile_alone && !mhc::ws_supported((int)H))
                 return fail(MHC_ERR_UNSUPPORTED, "H=%lld does not fit the ws schedule", (long long)H);
+            if (tile_alone && !mhc::tile_supported(T, H))
+                return fail(MHC_ERR_UNSUPPORTED, "the tile schedule needs H %% 64 == 0 and H > 256 (H=%lld)",
+                            (long long)H);
             mhc::FusedArgs a{};
             a.R = residual; a.Y = layer_out; a.prev_post = prev_post_mix; a.prev_comb = prev_comb_res_mix;
             a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
@@ -234,18 +267,41 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                                                : reinterpret_cast<uint4 *>(ws);
             a.prepacked = packed_phi != nullptr;
             float *zstash = reinterpret_cast<float *>(ws + ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)));
-            // with the bf16 layer input wanted as well, a separate streaming quantize pass over it
-            // is cheaper than ws's in-kernel epilogue (which lengthens the ring's critical chain);
-            // both give the same bits
+            a.redo_list = reinterpret_cast<unsigned int *>(zstash + (size_t)T * 16);
+            a.redo_len = T;
+            unsigned int *ctrl = static_cast<unsigned int *>(workspace);
+            // with the bf16 layer input wanted as well, a separate streaming quantize pass over it is
+            // cheaper than ws's in-kernel epilogue (which lengthens the ring's critical chain); both
+            // give the same bits
             const bool mx_pass = mx && layer_in_out != nullptr;
             a.mx = mx_pass ? mhc::MxOut{nullptr, nullptr, 0} : mxo;
-            e = mhc::launch_ws(a, static_cast<unsigned int *>(workspace), zstash, cs);
-            g_launches = a.prepacked ? 1 : 2;
+            if (tile_alone) {
+                // the token-tile kernel alone on every SM (with the packing launch before it)
+                if (!a.prepacked && (e = mhc::launch_ws_pack(phi, (int)H, a.phi_pack, cs)) != cudaSuccess) break;
+                e = mhc::launch_tile(a, 0, ctrl, zstash, dev.sms, false, cs);
+                g_launches = a.prepacked ? 1 : 2;
+            } else {
+                // AUTO on a large call: ws on the leading tokens, the token-tile kernel beside it on
+                // the SMs its clusters leave idle (side_split decides the share)
+                int side_ctas = 0;
+                const int64_t t_ws =
+                    forced_schedule() == MHC_SCHEDULE_WS ? T : side_split(T, H, fused, dev.sms, side_ctas);
+                const bool side = t_ws < T;
+                mhc::FusedArgs aw = a;
+                aw.T = t_ws;
+                aw.side_follows = side;
+                e = mhc::launch_ws(aw, ctrl, zstash, cs);
+                g_launches = a.prepacked ? 1 : 2;
+                if (e == cudaSuccess && side) {
+                    e = mhc::launch_tile(a, t_ws, ctrl, zstash, side_ctas, true, cs);
+                    mhc::mark_main_kernel(cs, false);
+                    g_launches += 1;
+                }
+            }
             if (e == cudaSuccess) {
-                // tokens whose streams cancel in X, listed by the ws kernel: layer input redone
+                // tokens whose streams cancel in X, listed by the kernels: layer input redone
                 e = mhc::launch_redo(fused ? residual_out : residual, rmsnorm_weight, rmsnorm_eps, T, (int)H,
-                                     pre_mix_out, layer_in_out, a.mx, static_cast<unsigned int *>(workspace),
-                                     reinterpret_cast<const unsigned int *>(zstash + (size_t)T * 16), cs);
+                                     pre_mix_out, layer_in_out, a.mx, ctrl, a.redo_list, cs);
                 g_launches += 1;
             }
             if (e == cudaSuccess && mx_pass) {
@@ -608,7 +664,7 @@ mhc_status mhc_pre_prepacked(const mhc_bf16 *residual, const float *phi, const v
 
 mhc_status mhc_set_schedule(int schedule) {
     if (schedule != MHC_SCHEDULE_AUTO && schedule != MHC_SCHEDULE_SPLIT && schedule != MHC_SCHEDULE_WS &&
-        schedule != MHC_SCHEDULE_SMALL && schedule != MHC_SCHEDULE_BCAST)
+        schedule != MHC_SCHEDULE_SMALL && schedule != MHC_SCHEDULE_BCAST && schedule != MHC_SCHEDULE_TILE)
         return fail(MHC_ERR_INVALID_ARG, "unknown schedule %d", schedule);
     g_forced_schedule.store(schedule, std::memory_order_relaxed);
     return MHC_OK;

@@ -66,6 +66,9 @@ struct FusedArgs {
     float *pre_out, *post_out, *res_out;
     uint4 *phi_pack;  // ws_pack_bytes(H): the workspace (packed by the call) or the caller's packed phi
     bool prepacked;   // phi_pack already holds the packed phi (no packing launch)
+    bool side_follows;  // ws: the token-tile kernel is launched right after it (beside it)
+    unsigned int *redo_list;  // [redo_len]: tokens whose layer input the redo pass recomputes
+    int64_t redo_len;         // the call's token count (ws may run on fewer, T above)
     MxOut mx;         // MXFP8 layer input (mx.q == nullptr: none)
 };
 
@@ -77,6 +80,16 @@ size_t ws_pack_bytes(int H);
 cudaError_t launch_ws_pack(const float *phi, int H, uint4 *out, cudaStream_t stream);
 size_t ws_stash_bytes(int64_t T);
 cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, cudaStream_t stream);
+// CTAs of ws resident at once on this device (clusters of 16 that fit, times 16).
+cudaError_t ws_resident_ctas(int H, bool post, int &ctas);
+
+// Token-tile schedule (kernels_tile.cu): tiles of 16 tokens, one CTA per SM, no clusters; phi
+// read from the ws packed form (a.phi_pack).  It computes tokens [t_begin, a.T) with up to
+// `grid` CTAs, alone or beside ws (beside: launched right after ws on the same stream, on the
+// SMs ws leaves idle).  The tokens whose streams cancel in X go on the redo list.
+bool tile_supported(int64_t T, int64_t H);
+cudaError_t launch_tile(const FusedArgs &a, int64_t t_begin, unsigned int *status, float *zstash, int grid,
+                        bool beside, cudaStream_t stream);
 
 // Small-T schedule (kernels_small.cu): one cooperative launch, one CTA per hidden slice,
 // grid barriers on 64-bit words at control-block bytes 64..71 (after the partial sums) and

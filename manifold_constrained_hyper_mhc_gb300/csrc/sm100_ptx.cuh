@@ -136,6 +136,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                                 uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4, %5}], [%6], %7;\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 // TMA tensor copy shared -> global (4-D box), in this thread's current bulk async-group.
 // Parts of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap *map, const void *src, int x, int y, int z, int w,

@@ -86,7 +86,7 @@ def test_broadcast_schedule_is_refused_where_it_cannot_run(mhc_lib):
                                    1 << 30, None) == -2
     finally:
         assert L.mhc_set_schedule(0) == 0
-    assert L.mhc_set_schedule(11) == -1                                           # unknown schedule
+    assert L.mhc_set_schedule(12) == -1                                           # unknown schedule
 
 
 def test_workspace_covers_the_broadcast_kernel(mhc_lib):
@@ -131,7 +131,7 @@ def test_removed_schedule_ids_are_refused(mhc_lib):
     L = mhc_lib.lib()
     for sid in range(2, 8):
         assert L.mhc_set_schedule(sid) == -1
-    for sid in (0, 1, 8, 9, 10):
+    for sid in (0, 1, 8, 9, 10, 11):
         assert L.mhc_set_schedule(sid) == 0
     assert L.mhc_set_schedule(0) == 0
 

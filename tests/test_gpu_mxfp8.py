@@ -93,7 +93,8 @@ def run_case(mhc, w, schedule, mode, gamma_decades=True, check_oracle=True):
 @pytest.mark.parametrize("schedule,T,H", [
     ("small", 6, 7168), ("small", 37, 1024), ("small", 1, 4096),
     ("ws", 6, 7168), ("ws", 130, 4096), ("ws", 300, 7168), ("ws", 9, 2080),
-    ("auto", 6, 7168), ("auto", 1000, 7168)])
+    ("tile", 40, 7168), ("tile", 300, 4096), ("tile", 7, 1088),
+    ("auto", 6, 7168), ("auto", 1000, 7168), ("auto", 2500, 7168)])
 def test_mxfp8_epilogue_matches_separate_quantize(mhc, schedule, T, H, mode):
     run_case(mhc, synth.Workload(f"mx_{schedule}_{T}x{H}", T, H, 300 + T, token_scale=True), schedule, mode)
 

@@ -53,6 +53,8 @@ SMALL_MAX_T = 128  # the small-T schedule takes T <= 128 (while its shared memor
 def check_workload(mhc, w, schedule="auto"):
     if schedule == "small" and (w.T > SMALL_MAX_T or (w.T > 96 and w.H > 4096)):
         pytest.skip("the small schedule takes T <= 128, and at H = 7168 T <= 96 (shared memory)")
+    if schedule == "tile" and (w.H % 64 != 0 or w.H <= 256):
+        pytest.skip("the tile schedule needs H % 64 == 0 and H > 256")
     (phi, bias, ms, gamma), wd = weights_dev(w)
     R, Y, pp, pc = synth.tokens(w)
     mhc.set_schedule(schedule)
@@ -65,7 +67,7 @@ def check_workload(mhc, w, schedule="auto"):
     assert not msgs, "\n".join(msgs)
 
 
-ALL_SCHEDULES = ["auto", "split", "ws", "small"]
+ALL_SCHEDULES = ["auto", "split", "ws", "small", "tile"]
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode_verify", "mid_batch"])
@@ -78,6 +80,32 @@ def test_workload_parity(mhc, name, schedule):
 @pytest.mark.parametrize("schedule", ALL_SCHEDULES)
 def test_ragged_shapes(mhc, T, H, schedule):
     check_workload(mhc, synth.Workload(f"ragged_{T}x{H}", T, H, 100 + T, token_scale=True), schedule)
+
+
+@pytest.mark.parametrize("T,H", [(1, 320), (17, 1088), (37, 2112), (130, 7168), (300, 4096), (1000, 7168)])
+def test_tile_schedule_shapes(mhc, T, H):
+    """The token-tile kernel alone on every SM: a single token, ragged tiles (T % 16 != 0) and
+    ragged chunks (H % 256 != 0), more tiles than SMs."""
+    check_workload(mhc, synth.Workload(f"tile_{T}x{H}", T, H, 200 + T, token_scale=True), "tile")
+
+
+@pytest.mark.parametrize("T,H", [(2048, 7168), (4096, 4096), (2500, 7168)])
+def test_ws_with_tile_beside(mhc, T, H):
+    """AUTO from 2048 tokens on: ws on the leading tokens, the token-tile kernel beside it on the
+    SMs ws's clusters leave idle; every token against the oracle, and the same results in place."""
+    w = synth.Workload(f"beside_{T}x{H}", T, H, 300 + T, token_scale=True)
+    check_workload(mhc, w)
+    (phi, bias, ms, gamma), wd = weights_dev(w)
+    R, Y, pp, pc = synth.tokens(w)
+    Rd = dev_bf16(R)
+    a = mhc.shifted_post_pre(dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC)
+    b = mhc.shifted_post_pre(Rd, dev_bf16(Y), dev_f32(pp), dev_f32(pc), *wd, **SC, out={"residual_out": Rd})
+    torch.cuda.synchronize()
+    for k in a:
+        x, y = a[k], b[k]
+        if x.dtype == torch.bfloat16:
+            x, y = x.view(torch.int16), y.view(torch.int16)
+        assert torch.equal(x, y), k
 
 
 def _full_parity(mhc, w, step=1024):

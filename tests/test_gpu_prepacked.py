@@ -35,7 +35,8 @@ def _same(a, b):
 
 
 @pytest.mark.parametrize("schedule,T,H", [("auto", 300, 7168), ("ws", 130, 4096), ("ws", 45, 2056),
-                                          ("auto", 6, 7168), ("split", 40, 7168), ("ws", 8192, 7168)])
+                                          ("auto", 6, 7168), ("split", 40, 7168), ("ws", 8192, 7168),
+                                          ("auto", 8192, 7168), ("tile", 300, 4096)])
 def test_prepacked_equals_plain(mhc, schedule, T, H):
     w = synth.Workload(f"pk_{T}x{H}", T, H, 700 + T)
     toks, wts = _args(w)
@@ -55,7 +56,7 @@ def test_prepacked_equals_plain(mhc, schedule, T, H):
         mhc.set_schedule("auto")
     _same(a, b)
     _same(c, d)
-    if ran == mhc.SCHEDULES["ws"]:
+    if ran in (mhc.SCHEDULES["ws"], mhc.SCHEDULES["tile"]):
         assert nb == na - 1  # no packing launch
 
 
