@@ -127,9 +127,9 @@ int forced_schedule() { return g_forced_schedule.load(std::memory_order_relaxed)
 // The token-tile kernel beside ws: below this many tokens (or with fewer idle SMs) ws runs alone.
 constexpr int64_t kSideMinT = 2048;
 constexpr int kSideMinSms = 8;
-// Measured per-SM rate of the token-tile kernel relative to ws's (prefill chunk, T = 8192,
-// H = 7168, both running together).
-constexpr double kSideRate = 0.55;
+// Per-SM rate of the token-tile kernel relative to ws's while both run (long prefill, T = 65536,
+// H = 7168: the split at which both kernels end together).
+constexpr double kSideRate = 0.635;
 
 // The first token of the token-tile kernel's share (T: ws alone), and in `idle` the SMs ws leaves
 // idle (the tile kernel's grid).  The share follows the two
