@@ -106,32 +106,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = pack2_rn(x0 - h0, x1 - h1);
 }
 
-// Grid barrier on one 64-bit word: the low 32 bits count the CTAs that have arrived, the high
-// 32 bits count the barriers completed on this word.  Called by one thread of each of the n CTAs.
-// Every CTA adds 1 (release); the CTA whose add makes the count n is the last, and it then adds
-// 2^32 - n, which returns the count to zero and advances the generation in one atomic.  A CTA
-// waits (acquire) until it sees either the count equal to n or the generation moved, so the barrier
-// opens as soon as the last arrival lands, and the reset is off that path.  A completed barrier
-// leaves the count at zero whatever n was, so calls with different CTA counts (different H) can
-// share the word; within one launch each barrier has its own word (a CTA may arrive at the next
-// barrier before the last one's reset of the previous one lands).  Bounded in time: on a
-// timeout it returns false; the CTA has still arrived, so the word stays consistent.
-__device__ bool grid_barrier(unsigned long long *word, unsigned int n) {
-    unsigned long long old, cur;
-    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(word) : "memory");
-    if ((unsigned int)(old & 0xFFFFFFFFull) == n - 1u) {
-        const unsigned long long step = (1ull << 32) - n;
-        asm volatile("red.add.relaxed.gpu.u64 [%0], %1;" ::"l"(word), "l"(step) : "memory");
-    }
-    const unsigned int gen = (unsigned int)(old >> 32);
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(word) : "memory");
-        if ((unsigned int)(cur & 0xFFFFFFFFull) == n || (unsigned int)(cur >> 32) != gen) return true;
-        if (globaltimer_ns() - t0 > kSpinLimitNs) return false;
-    }
-}
-
 // Warp-wide sum over the CTAs of 16 adjacent values, src[q * stride + 0..15] for CTA
 // q < nc (16-byte aligned rows).  Lane (quad j4 = lane & 3, group g = lane >> 2) adds
 // CTAs q = g, g + 8, g + 16, ... in that order from zero (its loads issued together,
@@ -371,7 +345,9 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
 
     // ---- 3. every CTA's records are in
     __syncthreads();
-    if (tid == 0) sFlag[0] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 16), (unsigned int)nc) ? 1 : 0;
+    if (tid == 0)
+        sFlag[0] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + kSmallBarrierWord), (unsigned int)nc,
+                                kSpinLimitNs) ? 1 : 0;
     __syncthreads();
     if (!sFlag[0]) {
         if (tid == 0) atomicOr(ctrl, 1u);
@@ -488,7 +464,9 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
             if (lane == 0) fixrec[(size_t)t * nc + c] = a;
         }
         wsync();
-        if (wt == 0) sFlag[2] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + 18), (unsigned int)nc) ? 1 : 0;
+        if (wt == 0)
+            sFlag[2] = grid_barrier(reinterpret_cast<unsigned long long *>(ctrl + kSmallBarrierWord + 2),
+                                    (unsigned int)nc, kSpinLimitNs) ? 1 : 0;
         wsync();
         if (!sFlag[2]) {
             if (wt == 0) atomicOr(ctrl, 1u);

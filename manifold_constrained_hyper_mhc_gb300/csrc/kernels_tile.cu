@@ -30,7 +30,9 @@
 //
 // Launched beside ws (programmatic dependent launch after it, so that ws's clusters are placed
 // first), it never waits for ws while it works; at its very end it waits for ws's completion
-// (griddepcontrol.wait), so whatever follows it on the stream sees both kernels' outputs.
+// (griddepcontrol.wait), so whatever follows it on the stream sees both kernels' outputs.  The
+// last CTA to finish then redoes the layer input of the tokens whose streams cancel in X (listed
+// by both kernels; see redo_token), so no separate redo launch follows.
 #include <cuda.h>
 
 #include <algorithm>
@@ -102,7 +104,8 @@ struct TLayout {
     __host__ __device__ static constexpr size_t head() { return gram() + (size_t)2 * kTT * 12 * 4; }       // [2][kTT][8]
     // full, postd, empty [kNSlot]; mixfull, mixempty, gfull, hfull [2]
     __host__ __device__ static constexpr size_t bars() { return head() + (size_t)2 * kTT * 8 * 4; }
-    __host__ __device__ static constexpr size_t bytes() { return bars() + (size_t)(3 * kNSlot + 8) * 8; }
+    __host__ __device__ static constexpr size_t flag() { return bars() + (size_t)(3 * kNSlot + 8) * 8; }  // u32
+    __host__ __device__ static constexpr size_t bytes() { return flag() + 16; }
 };
 
 struct TileMaps {
@@ -157,7 +160,8 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
             const float *__restrict__ mix_scales, const uint16_t *__restrict__ gamma, Scalars sc, int64_t t_begin,
             int64_t T, int H, int Hs_pack, uint16_t *__restrict__ X_out, float *__restrict__ pre_out,
             float *__restrict__ post_out, float *__restrict__ res_out, float *__restrict__ zstash,
-            unsigned int *__restrict__ redo_list, unsigned int *__restrict__ status, int wait_pack, MxOut mx) {
+            unsigned int *__restrict__ redo_list, unsigned int *__restrict__ status, int wait_pack, MxOut mx,
+            const uint16_t *__restrict__ Rp) {
     // a kernel after this one (the redo pass) may be scheduled now; it waits for this grid
     asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -588,8 +592,31 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
         for (int x = 0; x < 4; ++x) ro[x] = make_float4(M[4 * x], M[4 * x + 1], M[4 * x + 2], M[4 * x + 3]);
     }
     if (__any_sync(0xffffffffu, dead) && lane == 0) atomicOr(status, 1u);
-    // beside ws: this grid completes only after ws has (what follows on the stream sees both)
+    // ---- the redo pass: the layer input of the tokens whose streams cancel in X (listed by this
+    // kernel's heads and by ws's owners), redone by the last CTA of the grid to get here once ws
+    // is complete.  Each CTA counts itself done after its own tokens are listed.
+    unsigned int &sLast = *reinterpret_cast<unsigned int *>(smem + TLayout::flag());
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        sLast = atomicAdd(status + kRedoDoneWord, 1u) == gridDim.x - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    // beside ws: this grid completes only after ws has (what follows on the stream sees both), and
+    // ws's list entries and outputs are visible from here on
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!sLast) return;
+    __threadfence();
+    // (a list longer than the call's tokens can only be left over from an aborted call)
+    const unsigned int n0 = *reinterpret_cast<volatile unsigned int *>(status + kRedoCountWord);
+    const unsigned int n = n0 < (unsigned int)T ? n0 : (unsigned int)T;
+    for (unsigned int i = (unsigned int)warp; i < n; i += kNT / 32)
+        redo_token(Rp, gamma, sc.rmsnorm_eps, H, pre_out, X_out, mx, (int64_t)__ldcg(redo_list + i));
+    __syncthreads();
+    if (tid == 0) {
+        status[kRedoCountWord] = 0u;
+        status[kRedoDoneWord] = 0u;
+    }
 }
 
 }  // namespace
@@ -665,13 +692,14 @@ cudaError_t launch_tile(const FusedArgs &a, int64_t t_begin, unsigned int *statu
     cfg.numAttrs = (beside || !a.prepacked) ? 1 : 0;
     const int Hs_pack = ws_slice(a.H);
     unsigned int *list = a.redo_list;
+    const uint16_t *Rp = post ? a.R_out : a.R;  // R' for the redo pass in the kernel's tail
     if (!beside) mark_main_kernel(stream, true);
     e = post ? cudaLaunchKernelEx(&cfg, tile_kernel<true>, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales,
                                   a.gamma, a.s, t_begin, a.T, a.H, Hs_pack, a.X_out, a.pre_out, a.post_out, a.res_out,
-                                  zstash, list, status, (!beside && !a.prepacked) ? 1 : 0, a.mx)
+                                  zstash, list, status, (!beside && !a.prepacked) ? 1 : 0, a.mx, Rp)
              : cudaLaunchKernelEx(&cfg, tile_kernel<false>, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales,
                                   a.gamma, a.s, t_begin, a.T, a.H, Hs_pack, a.X_out, a.pre_out, a.post_out, a.res_out,
-                                  zstash, list, status, (!beside && !a.prepacked) ? 1 : 0, a.mx);
+                                  zstash, list, status, (!beside && !a.prepacked) ? 1 : 0, a.mx, Rp);
     if (!beside) mark_main_kernel(stream, false);
     return e;
 }

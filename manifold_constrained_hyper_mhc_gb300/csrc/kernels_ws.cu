@@ -10,8 +10,9 @@
 //   post (7 warps)    : the group's (token, 8-value vector) items, two per
 //                       thread; R' = comb^T R + post Y in shared memory (R'
 //                       overwrites R), R' to HBM.
-//   projection (8)    : warp p: tensor-memory lane quadrant p % 4, half of
-//                       that quadrant's quarter of the slice, all four streams.
+//   projection (7)    : warp p: tensor-memory lane quadrant (p + 7) % 4, a
+//                       share of the slice's 16-wide blocks (at most four), all
+//                       four streams.
 //                       Per 16 hidden values two ldmatrix.x4 load the 8 tokens'
 //                       R' of streams (0,1) and (2,3); the same fragments are the
 //                       B operand of the projection (A = phi^T hi/lo fragments
@@ -19,18 +20,20 @@
 //                       accumulate) and both operands of six Gram-matrix MMAs
 //                       (R'_i . R'_j over the hidden values for the stream
 //                       pairs, of which each token keeps its own diagonal
-//                       entries).  The eight warps' partials are summed into one
-//                       144-byte record per token (24 logits + 10 Gram entries)
-//                       and sent to the token's owner CTA (st.async).
+//                       entries).  Each warp writes its partials to shared
+//                       memory.
+//   sender (1 warp)   : sums the seven warps' partials into one 144-byte record
+//                       per token (24 logits + 10 Gram entries), sends it to the
+//                       token's owner CTA (st.async), and refills the Y ring.
 //   owner (1 warp)    : for the token this CTA owns in the group: sum the 16
 //                       records, r, the pre and post heads, rstd of the combined
 //                       row from the Gram matrix (sum_h X^2 = pre^T G pre),
 //                       (pre, rstd) to all 16 CTAs; residual-mix logits kept.
 //   combine (4 warps) : X = sum_i pre_i R'_i, RMSNorm * gamma, bf16 to HBM;
-//                       then, the slot's last use being over, one thread issues
-//                       the TMA tensor copies of group q + 5 into it (R as
-//                       64 x 8 x 4 boxes of 4 KB, Y as 64 x 8 boxes, the
-//                       previous mixes).
+//                       then, the slot's last use being over, the four warps
+//                       issue the TMA tensor copies of group q + 6 into it (R
+//                       as 64 x 8 x 4 boxes of 4 KB; the sender copies Y as
+//                       64 x 8 boxes and the previous mixes into the Y ring).
 // At the end all warps run the Sinkhorn normalisations of the owned tokens,
 // one token per thread.
 //
@@ -38,8 +41,8 @@
 // that used it (which comes after that group's post and projection).  The
 // owner's record buffer has two slots (its owned groups alternate); records
 // of group q are sent only after (pre, rstd) of group q-4 arrived, which the
-// owner sends after reading the slot.  The (pre, rstd) slots are 5 deep, and a
-// group can only reach them after the combine of the group 5 earlier.
+// owner sends after reading the slot.  The (pre, rstd) slots are 6 deep, and a
+// group can only reach them after the combine of the group 6 earlier.
 //
 // Every mbarrier wait is bounded: on a timeout the CTA sets bit 0 of the
 // status word and stops waiting (later waits give up at once), issues no more
@@ -283,6 +286,16 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     __syncthreads();
     tmem_fence_after();
     const uint32_t tbase = *sTmem;
+    // Up to here the kernel has touched only its own shared and tensor memory.  It is launched with
+    // programmatic dependent launch, so this set-up may overlap the end of the launch before it on
+    // the stream; from here on it reads and writes global memory, which that launch (the previous
+    // call's kernels, the packing launch, or whatever else came before) may still be using: wait for
+    // its completion.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the launches after this one (the token-tile kernel on the SMs the clusters leave idle, the
+    // redo pass) may start now: they read the packed phi, complete by now, and neither waits for
+    // this kernel before its end
+    asm volatile("griddepcontrol.launch_dependents;");
     // projection warp p = warp - kWP2 keeps the phi^T fragments of its blocks in tensor-memory
     // lane quadrant warp % 4, after those of the lower projection warps of the same quadrant:
     // block i, stream j at column col0 + (i*4 + j)*16 (3 x 4 registers of k16 step
@@ -295,13 +308,6 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             if (((p2 + kWP2) & 3) == (warp & 3)) col0 += 64 * nblk(p2);
         tq = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col0;
         const uint4 *pack = phi_pack + (size_t)c * (kHC * Hs / 16) * 96;
-        // the kernel may start while the packing launch before it still runs (programmatic
-        // dependent launch): wait for its results here, the only place that reads them
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        // the launches after this one (the token-tile kernel on the SMs the clusters leave idle,
-        // the redo pass) may start now: the packed phi they read is complete, and neither waits
-        // for this kernel before its end
-        asm volatile("griddepcontrol.launch_dependents;");
         for (int i = 0; i < nblk(p); ++i) {
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
@@ -919,13 +925,14 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
     attr[0].val.clusterDim.x = kC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // overlap the start (shared-memory and barrier setup, the first tile loads) with the
-    // packing launch; the projection warps wait for the packed phi (griddepcontrol.wait)
+    // programmatic dependent launch: the set-up (barriers, tensor memory) overlaps the end of the
+    // launch before this one (the packing launch, or the previous call's last kernel); the kernel
+    // waits for that launch's completion (griddepcontrol.wait) before it touches global memory
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kNT);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cfg.stream = stream;
     // one CTA per SM (the kernel takes all 512 tensor-memory columns): always ask for
     // more than half of the SM's shared memory
@@ -947,10 +954,6 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
         }
         cfg.gridDim = dim3((unsigned)(std::min<int64_t>((a.T + kG - 1) / kG, mc) * kC));
     }
-    // with the packing launch before it, overlap the two (the projection warps wait for the packed
-    // phi); with phi packed by the caller there is nothing to overlap, and the kernel reads its
-    // inputs from its first instruction, so it is launched in plain stream order
-    cfg.numAttrs = a.prepacked ? 1 : 2;
     mark_main_kernel(stream, true);
     e = cudaLaunchKernelEx(&cfg, kern, maps, (const uint4 *)a.phi_pack, a.bias, a.mix_scales, a.gamma, a.s, a.T,
                            a.H, Hs, lay, a.R_out, a.X_out, a.pre_out, a.post_out, a.res_out, zstash, a.redo_list,

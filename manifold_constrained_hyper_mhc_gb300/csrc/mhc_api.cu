@@ -275,11 +275,13 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             // give the same bits
             const bool mx_pass = mx && layer_in_out != nullptr;
             a.mx = mx_pass ? mhc::MxOut{nullptr, nullptr, 0} : mxo;
+            bool tile_ran = false;  // the token-tile kernel's tail does the redo pass
             if (tile_alone) {
                 // the token-tile kernel alone on every SM (with the packing launch before it)
                 if (!a.prepacked && (e = mhc::launch_ws_pack(phi, (int)H, a.phi_pack, cs)) != cudaSuccess) break;
                 e = mhc::launch_tile(a, 0, ctrl, zstash, dev.sms, false, cs);
                 g_launches = a.prepacked ? 1 : 2;
+                tile_ran = true;
             } else {
                 // AUTO on a large call: ws on the leading tokens, the token-tile kernel beside it on
                 // the SMs its clusters leave idle (side_split decides the share)
@@ -296,10 +298,11 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
                     e = mhc::launch_tile(a, t_ws, ctrl, zstash, side_ctas, true, cs);
                     mhc::mark_main_kernel(cs, false);
                     g_launches += 1;
+                    tile_ran = true;
                 }
             }
-            if (e == cudaSuccess) {
-                // tokens whose streams cancel in X, listed by the kernels: layer input redone
+            if (e == cudaSuccess && !tile_ran) {
+                // tokens whose streams cancel in X, listed by ws: layer input redone
                 e = mhc::launch_redo(fused ? residual_out : residual, rmsnorm_weight, rmsnorm_eps, T, (int)H,
                                      pre_mix_out, layer_in_out, a.mx, ctrl, a.redo_list, cs);
                 g_launches += 1;

@@ -354,4 +354,60 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// The layer input of token t redone with a direct square sum (the fix-up of a token whose streams
+// cancel in X, see gram_cancels), by one warp: X from the updated residual Rp (the combine's fp32
+// expression), sum_h X^2 summed by each lane over its blocks of 32 values in order and then an
+// xor tree, the RMSNorm with that rstd, the bf16 row (when X_out is given) and its MXFP8 form (when
+// mx.q is given; H % 32 == 0).
+__device__ __forceinline__ void redo_token(const uint16_t *__restrict__ Rp, const uint16_t *__restrict__ gamma,
+                                           float rmsnorm_eps, int H, const float *__restrict__ pre_out,
+                                           uint16_t *__restrict__ X_out, const MxOut &mx, int64_t t) {
+    const int lane = threadIdx.x & 31;
+    const int nb32 = (H + 31) / 32;  // blocks of 32 values: block b holds vectors 4b .. 4b+3
+    // R' and pre through L2 only (the token-tile kernel redoes tokens whose R' and pre other CTAs of
+    // its own grid wrote)
+    const uint16_t *row = Rp + t * kHC * (int64_t)H;
+    const float4 p4 = __ldcg(reinterpret_cast<const float4 *>(pre_out + t * 4));
+    const float pre[kHC] = {p4.x, p4.y, p4.z, p4.w};
+    auto xvec = [&](int v, float (&x)[8]) {
+        float rf[kHC][8];
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) unpack8(__ldcg(reinterpret_cast<const uint4 *>(row + (int64_t)j * H + v * kVec)), rf[j]);
+        combine_vec8_x2(rf, pre, x);
+    };
+    float a = 0.f;
+    for (int b = lane; b < nb32; b += 32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int v = 4 * b + k;
+            if (v * kVec < H) {
+                float x[8];
+                xvec(v, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a = fmaf(x[e], x[e], a);
+            }
+        }
+    }
+    a = warp_sum(a);
+    const float rstd = __frsqrt_rn(fmaxf(a, 0.f) * (1.f / (float)H) + rmsnorm_eps);
+    for (int b = lane; b < nb32; b += 32) {
+        uint4 ob[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int v = 4 * b + k;
+            ob[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (v * kVec < H) {
+                float x[8];
+                xvec(v, x);
+                ob[k] = norm_vec8(x, rstd, ld_ro(gamma + v * kVec));
+                if (X_out != nullptr) st_stream(X_out + t * (int64_t)H + v * kVec, ob[k]);
+            }
+        }
+        if (mx.q != nullptr) {  // H % 32 == 0: the block is whole
+            const int jj[4] = {0, 1, 2, 3};
+            mx_quantize_block(ob, jj, mx.mode, mx.q + t * (int64_t)H + 32 * b, mx.scale + mx_scale_offset(t, b, H));
+        }
+    }
+}
+
 }  // namespace mhc

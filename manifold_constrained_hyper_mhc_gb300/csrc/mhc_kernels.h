@@ -18,8 +18,12 @@ constexpr int kPartStride = 32;  // floats per (token, chunk) record: z[24], squ
 // (device status word, barrier counters).
 constexpr size_t kControlBytes = 256;
 // 32-bit words of the control block: the length of the redo list (tokens whose streams cancel
-// in X, see redo_kernel) and the count of redo CTAs done; both zero between calls.
+// in X, see redo_kernel) and the count of CTAs done (the redo kernel's, or the token-tile
+// kernel's); both zero between calls.
 constexpr int kRedoCountWord = 32, kRedoDoneWord = 33;
+// The small schedule's two 64-bit grid-barrier words start at these 32-bit word offsets (16-17
+// and 18-19); each is zero in its low half between launches.
+constexpr int kSmallBarrierWord = 16;
 
 // A second stream for the off-critical-path part of a split call: `fork` is recorded on the
 // main stream once the records are in, the side stream waits on it, and `join` is recorded on

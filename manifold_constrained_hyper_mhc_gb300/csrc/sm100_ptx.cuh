@@ -255,5 +255,31 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Grid barrier on one 64-bit word: the low 32 bits count the CTAs that have arrived, the high
+// 32 bits count the barriers completed on this word.  Called by one thread of each of the n CTAs
+// (all resident at once).  Every CTA adds 1 (release); the CTA whose add makes the count n is the
+// last, and it then adds 2^32 - n, which returns the count to zero and advances the generation in
+// one atomic.  A CTA waits (acquire) until it sees either the count equal to n or the generation
+// moved, so the barrier opens as soon as the last arrival lands, and the reset is off that path.
+// A completed barrier leaves the count at zero whatever n was, so launches with different CTA
+// counts can share the word; within one launch each barrier has its own word (a CTA may arrive at
+// the next barrier before the last one's reset of the previous one lands).  Bounded in time: after
+// limit_ns it returns false; the CTA has still arrived, so the word stays consistent.
+__device__ __forceinline__ bool grid_barrier(unsigned long long *word, unsigned int n, uint64_t limit_ns) {
+    unsigned long long old, cur;
+    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(word) : "memory");
+    if ((unsigned int)(old & 0xFFFFFFFFull) == n - 1u) {
+        const unsigned long long step = (1ull << 32) - n;
+        asm volatile("red.add.relaxed.gpu.u64 [%0], %1;" ::"l"(word), "l"(step) : "memory");
+    }
+    const unsigned int gen = (unsigned int)(old >> 32);
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(cur) : "l"(word) : "memory");
+        if ((unsigned int)(cur & 0xFFFFFFFFull) == n || (unsigned int)(cur >> 32) != gen) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 }  // namespace ptx
 }  // namespace mhc
