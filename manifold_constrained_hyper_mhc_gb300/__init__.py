@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "MhcError", "lib", "workspace_size", "new_workspace", "shifted_post_pre", "post", "pre",
-    "set_schedule", "auto_schedule", "check_status", "last_launch_count", "SCHEDULES",
+    "set_schedule", "auto_schedule", "auto_side_tokens", "check_status", "last_launch_count", "SCHEDULES",
     "post_int8", "post_sqrsum", "pre_broadcast", "shifted_post_pre_split", "shifted_post_pre_mxfp8", "mxfp8_scale_bytes", "MX_SCALE_FLOOR", "MX_SCALE_CEIL", "set_main_kernel_events",
     "packed_phi_bytes", "pack_phi",
 ]
@@ -87,6 +87,8 @@ def lib():
             L.mhc_set_schedule.restype = I
             L.mhc_auto_schedule.argtypes = [I64, I64]
             L.mhc_auto_schedule.restype = I
+            L.mhc_auto_side_tokens.argtypes = [I64, I64]
+            L.mhc_auto_side_tokens.restype = I64
             L.mhc_check_status.argtypes = [P, P]
             L.mhc_check_status.restype = I
             L.mhc_status_string.argtypes = [I]
@@ -392,6 +394,12 @@ def set_schedule(name_or_id):
 
 def auto_schedule(T: int, H: int) -> int:
     return int(lib().mhc_auto_schedule(int(T), int(H)))
+
+
+def auto_side_tokens(T: int, H: int) -> int:
+    """How many trailing tokens of a fused AUTO call the token-tile kernel takes beside ws (0: ws
+    alone); -1 without a CUDA device."""
+    return int(lib().mhc_auto_side_tokens(int(T), int(H)))
 
 
 def last_launch_count() -> int:

@@ -132,10 +132,9 @@ constexpr int kSideMinSms = 8;
 constexpr double kSideRate = 0.635;
 
 // The first token of the token-tile kernel's share (T: ws alone), and in `idle` the SMs ws leaves
-// idle (the tile kernel's grid).  The share follows the two
-// kernels' rates (ws on its resident CTAs, the tile kernel on the idle SMs) and is a whole number
-// of 16-token tiles per idle SM, so the tile kernel's CTAs finish together; ws keeps whole groups
-// of 8 tokens.
+// idle (the tile kernel's grid).  The share follows the two kernels' rates (ws on its resident
+// CTAs, the tile kernel on the idle SMs) and is a whole number of 16-token tiles per idle SM, so
+// the tile kernel's CTAs finish together; ws keeps whole groups of 8 tokens.
 int64_t side_split(int64_t T, int64_t H, bool fused, int sms, int &idle) {
     idle = 0;
     if (T < kSideMinT || !mhc::tile_supported(T, H)) return T;
@@ -677,6 +676,15 @@ int mhc_auto_schedule(int64_t T, int64_t H) {
     Device dev;
     if (current_device(dev) != MHC_OK) return MHC_SCHEDULE_AUTO;
     return auto_schedule(T, H, dev.sms);
+}
+
+int64_t mhc_auto_side_tokens(int64_t T, int64_t H) {
+    if (T < 0 || H < 0) return -1;
+    Device dev;
+    if (current_device(dev) != MHC_OK) return -1;
+    if (auto_schedule(T, H, dev.sms) != MHC_SCHEDULE_WS) return 0;
+    int idle = 0;
+    return T - side_split(T, H, true, dev.sms, idle);
 }
 
 mhc_status mhc_check_status(void *workspace, void *stream) {
