@@ -448,9 +448,6 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 mma_acc<kF>(gd[0], f[0], f[2], f[1], f[3], f[0], f[1]);
                 mma_acc<kF>(gd[1], f[0], f[2], f[1], f[3], f[2], f[3]);
                 mma_acc<kF>(gd[2], f[0], f[2], f[1], f[3], g[0], g[1]);
-                mma_acc<kF>(gd[3], f[0], f[2], f[1], f[3], g[2], g[3]);
-                mma_acc<kF>(gd[4], g[0], g[2], g[1], g[3], g[0], g[1]);
-                mma_acc<kF>(gd[5], g[0], g[2], g[1], g[3], g[2], g[3]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt)
@@ -460,6 +457,10 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                     mma_bf16(acc[mt], a[12 + 4 * mt], a[13 + 4 * mt], a[14 + 4 * mt], a[15 + 4 * mt], f[2], f[3]);
                 tmem_ld12(tq + (uint32_t)((i * 4 + 2) * 16), a);
                 tmem_ld12(tq + (uint32_t)((i * 4 + 3) * 16), a + 12);
+                // the rest of the Gram tiles cover the second tensor-memory load
+                mma_acc<kF>(gd[3], f[0], f[2], f[1], f[3], g[2], g[3]);
+                mma_acc<kF>(gd[4], g[0], g[2], g[1], g[3], g[0], g[1]);
+                mma_acc<kF>(gd[5], g[0], g[2], g[1], g[3], g[2], g[3]);
                 tmem_wait_ld();
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt)
