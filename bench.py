@@ -537,8 +537,8 @@ def run_ours(args, rank, world, lr, dist):
         sched = args.schedule
     elif args.op in ("fused", "split", "pre"):
         sched = auto_name
-        if args.op == "fused" and auto_name == "ws":
-            side_tokens = mhc.auto_side_tokens(T, H)
+        if args.op in ("fused", "pre") and auto_name == "ws":
+            side_tokens = mhc.auto_side_tokens(T, H, args.op == "fused")
             if side_tokens > 0:  # the token-tile kernel beside ws on the SMs its clusters leave idle
                 sched = "ws+tile"
     elif args.op == "pre_broadcast":  # the fused kernel from x alone above 32 tokens, else residual + pre
@@ -564,7 +564,9 @@ def run_ours(args, rank, world, lr, dist):
                    "call_gbs": abytes / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if whole_call else
-                     measured_traffic(sched if mx_mode is None else sched + "_mxfp8_only", w.name, T, H), "peak_source": peak_src,
+                     measured_traffic((sched if args.op != "pre" else "pre_" + sched)
+                                      + ("" if mx_mode is None else "_mxfp8_only"), w.name, T, H),
+                     "peak_source": peak_src,
                      "kernel": (f"whole call ({launches} launches), {ms_step * 1e3:.1f} us; main kernel "
                                 f"{kernel_ms * 1e3:.1f} us" if whole_call else
                                 f"main span of the call ({launches} launches per call, all of them the main "

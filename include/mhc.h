@@ -342,11 +342,12 @@ MHC_API mhc_status mhc_set_schedule(int schedule);
 /* The schedule AUTO would pick for (T, H) on the current device. */
 MHC_API int mhc_auto_schedule(int64_t T, int64_t H);
 
-/* For a fused call (mhc_shifted_post_pre) of T tokens, hidden size H on the current device that
- * AUTO runs on the ws schedule: the number of trailing tokens the token-tile kernel takes beside
- * ws, on the SMs ws's 16-CTA clusters leave idle (0 when ws runs alone).  Returns -1 when T or H
- * is negative or no CUDA device is current.  Changes nothing; a planning query. */
-MHC_API int64_t mhc_auto_side_tokens(int64_t T, int64_t H);
+/* For a call of T tokens, hidden size H on the current device that AUTO runs on the ws schedule
+ * (fused != 0: mhc_shifted_post_pre and its variants; fused == 0: mhc_pre): the number of
+ * trailing tokens the token-tile kernel takes beside ws, on the SMs ws's 16-CTA clusters leave
+ * idle (0 when ws runs alone or AUTO picks another schedule).  Returns -1 when T or H is negative
+ * or no CUDA device is current.  Changes nothing; a planning query. */
+MHC_API int64_t mhc_auto_side_tokens(int64_t T, int64_t H, int fused);
 
 /* Synchronises `stream`, then reads the device status word kept in the
  * workspace: MHC_ERR_DEVICE_TIMEOUT if a bounded device-side wait gave up since

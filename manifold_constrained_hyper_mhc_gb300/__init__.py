@@ -87,7 +87,7 @@ def lib():
             L.mhc_set_schedule.restype = I
             L.mhc_auto_schedule.argtypes = [I64, I64]
             L.mhc_auto_schedule.restype = I
-            L.mhc_auto_side_tokens.argtypes = [I64, I64]
+            L.mhc_auto_side_tokens.argtypes = [I64, I64, I]
             L.mhc_auto_side_tokens.restype = I64
             L.mhc_check_status.argtypes = [P, P]
             L.mhc_check_status.restype = I
@@ -396,10 +396,10 @@ def auto_schedule(T: int, H: int) -> int:
     return int(lib().mhc_auto_schedule(int(T), int(H)))
 
 
-def auto_side_tokens(T: int, H: int) -> int:
-    """How many trailing tokens of a fused AUTO call the token-tile kernel takes beside ws (0: ws
-    alone); -1 without a CUDA device."""
-    return int(lib().mhc_auto_side_tokens(int(T), int(H)))
+def auto_side_tokens(T: int, H: int, fused: bool = True) -> int:
+    """How many trailing tokens of an AUTO call (fused: shifted_post_pre; else pre) the token-tile
+    kernel takes beside ws (0: ws alone or another schedule); -1 without a CUDA device."""
+    return int(lib().mhc_auto_side_tokens(int(T), int(H), 1 if fused else 0))
 
 
 def last_launch_count() -> int:

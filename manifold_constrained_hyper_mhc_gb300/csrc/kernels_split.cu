@@ -219,6 +219,7 @@ cudaError_t launch_split(const SplitArgs &a, cudaStream_t stream) {
     const int nchunk = (a.H + kSplitH - 1) / kSplitH;
     const unsigned tblocks = (unsigned)((a.T + kSplitTok - 1) / kSplitTok);
     dim3 g1(tblocks, nchunk);
+    mark_main_kernel(stream, true);  // the main span: all three kernels
     if (a.R_out != nullptr)
         split_partials_kernel<true><<<g1, kThreads, 0, stream>>>(
             a.R, a.Y, a.prev_post, a.prev_comb, a.phi, a.T, a.H, a.R_out, a.part);
@@ -233,6 +234,7 @@ cudaError_t launch_split(const SplitArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     split_combine_kernel<<<(unsigned)a.T, kThreads, 0, stream>>>(
         a.R_out != nullptr ? a.R_out : a.R, a.gamma, a.pre_out, a.s.rmsnorm_eps, a.H, a.X_out);
+    mark_main_kernel(stream, false);
     return cudaGetLastError();
 }
 

@@ -296,6 +296,37 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
     // redo pass) may start now: they read the packed phi, complete by now, and neither waits for
     // this kernel before its end
     asm volatile("griddepcontrol.launch_dependents;");
+    // the first groups' copies go out now, ahead of the phi fill and the cluster barrier: they
+    // need only this CTA's barriers
+    if (warp >= kWCB && warp < kWCB + kCB && lane == 0) {
+        const int cw = warp - kWCB;
+        for (int q = 0; q < kNBuf && q < n_it; ++q) {
+            const int b = q % kNBuf;
+            const int t0 = (int)group_t0(q);
+            if (cw == 0) mbar_arrive_expect_tx(&full[b], (uint32_t)nHB * 4096);
+            unsigned char *rs = smem + L.r_off(b);
+            if (lay.one_box) {
+                tma_load_4d(rs + cw * lay.s_j, &maps.R, 0, t0, h0 / 64, cw, &full[b]);
+            } else {
+                for (int hb = cw; hb < nHB; hb += kCB) tma_load_3d(rs + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
+            }
+        }
+    }
+    if (kPost && warp == kWSend && lane == 0) {
+        const uint32_t ybytes = (uint32_t)nHB * 1024 + 512 + 128;
+        for (int q = 0; q < kNY && q < n_it; ++q) {
+            const int ys = q % kNY;
+            const int t0 = (int)group_t0(q);
+            mbar_arrive_expect_tx(&yfull[ys], ybytes);
+            if (lay.one_box)
+                tma_load_3d(smem + L.y_off(ys), &maps.Y, 0, t0, h0 / 64, &yfull[ys]);
+            else
+                for (int hb = 0; hb < nHB; ++hb)
+                    tma_load_2d(smem + L.y_off(ys) + hb * 1024, &maps.Y, h0 + hb * 64, t0, &yfull[ys]);
+            tma_load_2d(smem + L.comb_off(ys), &maps.comb, 0, t0, &yfull[ys]);
+            tma_load_2d(smem + L.post_off(ys), &maps.post, 0, t0, &yfull[ys]);
+        }
+    }
     // projection warp p = warp - kWP2 keeps the phi^T fragments of its blocks in tensor-memory
     // lane quadrant warp % 4, after those of the lower projection warps of the same quadrant:
     // block i, stream j at column col0 + (i*4 + j)*16 (3 x 4 registers of k16 step
@@ -528,8 +559,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
                 for (int hb = cw; hb < nHB; hb += kCB) tma_load_3d(rs + hb * 4096, &maps.R, h0 + hb * 64, t0, 0, &full[b]);
             }
         };
-        if (lane == 0)
-            for (int q = 0; q < kNBuf && q < n_it; ++q) issue(q);
+
         // token-major items: thread ct works on token ct / kCPT, vectors ct % kCPT + kCPT * k, so the
         // token's (pre, rstd) is read once per group; offsets computed once.  With the MXFP8 output
         // the thread instead takes the four vectors of block b = ct % kCPT (at most 14 blocks of
@@ -613,8 +643,7 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
             tma_load_2d(smem + L.comb_off(ys), &maps.comb, 0, t0, &yfull[ys]);
             tma_load_2d(smem + L.post_off(ys), &maps.post, 0, t0, &yfull[ys]);
         };
-        if (kPost && lane == 0)
-            for (int q = 0; q < kNY && q < n_it; ++q) issue_y(q);
+
         for (int q = 0; q < n_it; ++q) {
             bwait(&parts_ready[q & 1], (uint32_t)((q >> 1) & 1), dead);
             // chunk (token t, 16-byte piece qq) = lane + 32 k: sum of the warps' partials, fixed order

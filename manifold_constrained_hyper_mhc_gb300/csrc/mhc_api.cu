@@ -678,13 +678,13 @@ int mhc_auto_schedule(int64_t T, int64_t H) {
     return auto_schedule(T, H, dev.sms);
 }
 
-int64_t mhc_auto_side_tokens(int64_t T, int64_t H) {
+int64_t mhc_auto_side_tokens(int64_t T, int64_t H, int fused) {
     if (T < 0 || H < 0) return -1;
     Device dev;
     if (current_device(dev) != MHC_OK) return -1;
     if (auto_schedule(T, H, dev.sms) != MHC_SCHEDULE_WS) return 0;
     int idle = 0;
-    return T - side_split(T, H, true, dev.sms, idle);
+    return T - side_split(T, H, fused != 0, dev.sms, idle);
 }
 
 mhc_status mhc_check_status(void *workspace, void *stream) {
