@@ -1,16 +1,16 @@
-// Token-tile schedule (schedule "tile"): the whole fused mHC post+pre step for tiles of 16
+// Token-tile schedule (schedule "tile"): the whole fused mHC post+pre step for tiles of 18
 // tokens, one CTA per SM, no clusters.  It runs on its own (every SM, any H % 64 == 0), or
 // beside the ws schedule on the SMs that ws's 16-CTA clusters cannot use, on a share of the
 // tokens (ws takes the leading tokens, this kernel the rest).
 //
 // A tile's row (4 streams x H) does not fit in shared memory, so it is walked twice in chunks of
-// 16 tokens x 256 hidden values:
+// 18 tokens x 256 hidden values:
 //   pass 1: the post (R' = comb^T R + post Y, fp32, rounded to bf16) in shared memory, R' to HBM
 //           by a TMA store with the L2 evict-last policy; the 10 Gram entries per token
 //           (sum_h R'_i R'_j) in fp32 from the post's registers; the projection onto the 24
 //           logits on the tensor cores (mma.sync m16n8k16 bf16: A = phi^T as bf16 high part and
-//           remainder, the packed form of the ws schedule read from L2; B = R', the 16 tokens as
-//           two n8 tiles; fp32 accumulate);
+//           remainder, the packed form of the ws schedule read from L2; B = R', the 18 tokens as
+//           three n8 tiles, the last part-filled; fp32 accumulate);
 //   heads:  r, the pre and post mixes, rstd from the Gram matrix, the residual-mix logits kept
 //           for the Sinkhorn at the end of the kernel;
 //   pass 2: R' read back from L2, X = sum_i pre_i R'_i, RMSNorm * gamma, bf16 to HBM (and, when
@@ -18,7 +18,9 @@
 // Pass-2 chunks of tile k-1 are interleaved with pass-1 chunks of tile k (two chunks behind),
 // so the HBM reads of pass 1, the L2 reads of both passes and the heads overlap.  HBM moves
 // 20H + 176 bytes per token, as in the single-pass schedules; L2 additionally serves phi
-// (24 * 4H * 4 bytes per 16 tokens) and the R' re-read.
+// (24 * 4H * 4 bytes per tile) and the R' re-read.  18 tokens (not 16) per tile: the busiest
+// elementwise warp still takes three tokens, only the projection's third n8 tile is extra, and
+// the larger share per SM lets this kernel take more of a call's tokens beside ws.
 //
 // Roles (16 warps, so 128 registers a thread): 7 elementwise warps (the post in pass 1, the
 // combine in pass 2; warp w takes tokens w, w + 7, w + 14 of each chunk, lane v the chunk's
@@ -50,7 +52,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTT = 16;                         // tokens per tile: two n8 tiles of the MMAs
+constexpr int kTT = 18;                         // tokens per tile: three n8 tiles of the MMAs, the last part-filled
+constexpr int kNT8 = (kTT + 7) / 8;             // n8 tiles
 constexpr int kCW = 256;                        // hidden values per chunk
 constexpr int kCHB = kCW / 64;                  // 64-wide blocks per chunk (TMA box depth)
 constexpr int kRB = kHC * kCHB * kTT * 128;     // R or R' of a chunk: 32 KB
@@ -60,11 +63,13 @@ constexpr int kNSlot = 4;
 constexpr int kEW = 7, kPW = 8;                 // elementwise warps 0-6, projection warps 7-14
 constexpr int kWProd = kEW + kPW;               // warp 15: loads and stores (one thread)
 constexpr int kNT = (kWProd + 1) * 32;          // 16 warps: 4 per SM sub-partition, 128 registers
-constexpr int kItems = kTT * (kCW / kVec);      // (token, vector) items of a chunk: 512
-constexpr int kMixB = kTT * 64 + kTT * 16;      // comb [16][16] + post [16][4] fp32
+constexpr int kItems = kTT * (kCW / kVec);      // (token, vector) items of a chunk: 32 per token
+constexpr int kMixB = (kTT * 80 + 127) / 128 * 128;  // comb [kTT][16] + post [kTT][4] fp32, 128-byte aligned
 constexpr int kLag = 2;                         // pass-2 chunks trail pass-1 chunks by this many
 constexpr int kEmptyCount = kEW + kPW + 1;      // every role releases every slot (the producer too)
 constexpr uint64_t kWaitNs = 1000000000ull;
+static_assert(kSlot % 1024 == 0 && kRB % 1024 == 0, "ring slots and their Y part start on the swizzle period");
+static_assert(kTT <= 24 && kTT <= 32, "three n8 tiles at most; one head lane per token");
 
 __device__ __forceinline__ void bwait(uint64_t *bar, uint32_t parity, bool &dead) {
     mbar_wait_timed(bar, parity, dead, kWaitNs);
@@ -86,6 +91,13 @@ __device__ __forceinline__ uint4 ldg_keep(const uint4 *p, uint64_t policy) {
                  : "l"(p), "l"(policy));
     return v;
 }
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r[0]), "=r"(r[1]) : "r"(addr) : "memory");
+}
+// Byte offset of 16-byte chunk c16 of row `row` of a ring slot: TMA's 128-byte swizzle XORs the
+// chunk index with the row's position in its 1024-byte period (rows of 128 bytes, counted from the
+// slot's 1024-aligned start across the box's (stream, block) planes of kTT rows each)
+__device__ __forceinline__ uint32_t swz(int row, int c16) { return (uint32_t)(row * 128 + ((c16 ^ (row & 7)) << 4)); }
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -251,7 +263,7 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
                         if (lp == 0) {
                             if (kPost && lc == 0) {  // the tile's previous mixes, with its first chunk
                                 unsigned char *m = mixb + (size_t)(lk & 1) * kMixB;
-                                mbar_arrive_expect_tx(&mixfull[lk & 1], kMixB);
+                                mbar_arrive_expect_tx(&mixfull[lk & 1], kTT * 80);  // the two copies' bytes (the buffer is padded)
                                 tma_load_2d(m, &maps.comb, 0, t0, &mixfull[lk & 1]);
                                 tma_load_2d(m + kTT * 64, &maps.post, 0, t0, &mixfull[lk & 1]);
                             }
@@ -284,8 +296,8 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
         }
     } else if (warp < kEW) {
         // ================================ elementwise: the post (pass 1), the combine (pass 2).
-        // Item i = tid + 224 u (u = 0, 1, 2; i < 512) of a chunk: token i / 32, vector i % 32, so
-        // warp w takes tokens w, w + 7 and (w < 2) w + 14, lane v the chunk's vector v.
+        // Item i = tid + 224 u (u = 0, 1, 2; i < 32 kTT) of a chunk: token i / 32, vector i % 32, so
+        // warp w takes tokens w, w + 7 and (w < kTT - 14) w + 14, lane v the chunk's vector v.
         constexpr int kU = (kItems + kEW * 32 - 1) / (kEW * 32);  // 3
         float g[kU][10];  // Gram partials of the warp's tokens over the tile
 #pragma unroll
@@ -312,17 +324,14 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
                     uint4 r4[kHC];
 #pragma unroll
                     for (int j = 0; j < kHC; ++j)
-                        r4[j] = *reinterpret_cast<const uint4 *>(sl + ((j * kCHB + hb) * kTT + t) * 128 +
-                                                                 ((c16 ^ (t & 7)) << 4));
+                        r4[j] = *reinterpret_cast<const uint4 *>(sl + swz((j * kCHB + hb) * kTT + t, c16));
                     if (kPost) {
-                        const uint4 y = *reinterpret_cast<const uint4 *>(sl + kRB + (hb * kTT + t) * 128 +
-                                                                         ((c16 ^ (t & 7)) << 4));
+                        const uint4 y = *reinterpret_cast<const uint4 *>(sl + kRB + swz(hb * kTT + t, c16));
                         uint4 o[kHC];
                         post_vec8_x2(r4, y, mx + t * 16, mx + kTT * 16 + t * 4, o, rf);
 #pragma unroll
                         for (int j = 0; j < kHC; ++j)
-                            *reinterpret_cast<uint4 *>(sl + ((j * kCHB + hb) * kTT + t) * 128 + ((c16 ^ (t & 7)) << 4)) =
-                                o[j];
+                            *reinterpret_cast<uint4 *>(sl + swz((j * kCHB + hb) * kTT + t, c16)) = o[j];
                     } else {
 #pragma unroll
                         for (int j = 0; j < kHC; ++j) unpack8(r4[j], rf[j]);
@@ -393,9 +402,7 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
                         float rf[kHC][8], x[8];
 #pragma unroll
                         for (int j = 0; j < kHC; ++j)
-                            unpack8(*reinterpret_cast<const uint4 *>(sl + ((j * kCHB + hb) * kTT + t) * 128 +
-                                                                     ((c16 ^ (t & 7)) << 4)),
-                                    rf[j]);
+                            unpack8(*reinterpret_cast<const uint4 *>(sl + swz((j * kCHB + hb) * kTT + t, c16)), rf[j]);
                         combine_vec8_x2(rf, hp[u], x);
                         ob = norm_vec8(x, hr[u], ld_ro(gamma + h));
                         if (X_out != nullptr) st_stream(X_out + (t0 + t) * (int64_t)H + h, ob);
@@ -420,11 +427,11 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
         // ldmatrix.x4 rows: lanes 0-15 tokens 0-7 (k 0-7, then k 8-15), lanes 16-31 tokens 8-15
         const int lt = (lane & 7) + 8 * (lane >> 4), lk = ((lane >> 3) & 1) * 8;
         const int nsteps_pack = kHC * Hs_pack / 16;  // k16 steps per CTA slice of the packed phi
-        float acc[3][2][4];
+        float acc[3][kNT8][4];
 #pragma unroll
         for (int mt = 0; mt < 3; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < kNT8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
         // phi^T fragments: the packed form (ws's) holds, per CTA slice cr of Hs_pack hidden values and
@@ -478,13 +485,18 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
             for (int s = 0; s < 8; ++s) {
                 const int b = 2 * p + (s >> 2), j = s & 3;
                 const int hh = b * 16 + lk;  // hidden offset within the chunk of this lane's row
+                const int row0 = (j * kCHB + (hh >> 6)) * kTT, c16 = (hh & 63) >> 3;
                 uint32_t r[4];
-                ldsm_x4(sl + (uint32_t)(((j * kCHB + (hh >> 6)) * kTT + lt) * 128 + ((((hh & 63) >> 3) ^ (lt & 7)) << 4)),
-                        r);
+                ldsm_x4(sl + swz(row0 + lt, c16), r);
+                uint32_t r2[2];
+                // tokens 16-23 (lanes 0-15 give the rows; rows past the tile read the next plane's rows,
+                // inside the slot, and only feed columns that are dropped)
+                if (kNT8 > 2) ldsm_x2(sl + swz(row0 + 16 + (lane & 7), c16), r2);
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt) {
                     mma16816(acc[mt][0], fr[s & 3][mt], r[0], r[1]);
                     mma16816(acc[mt][1], fr[s & 3][mt], r[2], r[3]);
+                    if (kNT8 > 2) mma16816(acc[mt][2], fr[s & 3][mt], r2[0], r2[1]);
                 }
                 // refill this ring entry with the step four ahead
                 if (s < 4) frag(b1, s, fr[s & 3]);
@@ -498,10 +510,11 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
             // (two buffers, by tile parity)
             float *pw = sPart + (size_t)((k & 1) * kPW + p) * kTT * 24;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < kNT8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int t = nt * 8 + 2 * tig + e;
+                    if (t >= kTT) continue;
                     pw[t * 24 + gid] = acc[0][nt][e] + acc[1][nt][2 + e];
                     pw[t * 24 + gid + 8] = acc[0][nt][2 + e] + acc[2][nt][e];
                     pw[t * 24 + gid + 16] = acc[1][nt][e] + acc[2][nt][2 + e];
@@ -509,7 +522,7 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
 #pragma unroll
             for (int mt = 0; mt < 3; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int nt = 0; nt < kNT8; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
             named_sync(1, kPW * 32);
@@ -628,6 +641,8 @@ bool tile_supported(int64_t T, int64_t H) {
 }
 
 size_t tile_smem_bytes() { return TLayout::bytes() + 1024; }
+
+int tile_tokens() { return kTT; }
 
 cudaError_t launch_tile(const FusedArgs &a, int64_t t_begin, unsigned int *status, float *zstash, int grid,
                         bool beside, cudaStream_t stream) {

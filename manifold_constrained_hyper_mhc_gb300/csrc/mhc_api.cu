@@ -128,12 +128,13 @@ int forced_schedule() { return g_forced_schedule.load(std::memory_order_relaxed)
 constexpr int64_t kSideMinT = 2048;
 constexpr int kSideMinSms = 8;
 // Per-SM rate of the token-tile kernel relative to ws's while both run (long prefill, T = 65536,
-// H = 7168: the split at which both kernels end together).
-constexpr double kSideRate = 0.635;
+// H = 7168: the split at which both kernels end together; rates 0.50-0.58 gave the tile kernel
+// 15-16 rounds and 1,878-1,851 us, 0.62 gave it 17 rounds and made it the tail at 1,947 us).
+constexpr double kSideRate = 0.58;
 
 // The first token of the token-tile kernel's share (T: ws alone), and in `idle` the SMs ws leaves
 // idle (the tile kernel's grid).  The share follows the two kernels' rates (ws on its resident
-// CTAs, the tile kernel on the idle SMs) and is a whole number of 16-token tiles per idle SM, so
+// CTAs, the tile kernel on the idle SMs) and is a whole number of tiles per idle SM, so
 // the tile kernel's CTAs finish together; ws keeps whole groups of 8 tokens.
 int64_t side_split(int64_t T, int64_t H, bool fused, int sms, int &idle) {
     idle = 0;
@@ -143,7 +144,7 @@ int64_t side_split(int64_t T, int64_t H, bool fused, int sms, int &idle) {
     idle = sms - ws_ctas;
     if (idle < kSideMinSms) return T;
     const double f = idle * kSideRate / (ws_ctas + idle * kSideRate);
-    const int64_t per_round = (int64_t)idle * 16;
+    const int64_t per_round = (int64_t)idle * mhc::tile_tokens();
     const int64_t rounds = (int64_t)(T * f / per_round + 0.5);
     if (rounds < 1) return T;
     return (T - rounds * per_round) / 8 * 8;

@@ -92,6 +92,7 @@ cudaError_t ws_resident_ctas(int H, bool post, int &ctas);
 // `grid` CTAs, alone or beside ws (beside: launched right after ws on the same stream, on the
 // SMs ws leaves idle).  The tokens whose streams cancel in X go on the redo list.
 bool tile_supported(int64_t T, int64_t H);
+int tile_tokens();  // tokens per tile of the token-tile kernel
 cudaError_t launch_tile(const FusedArgs &a, int64_t t_begin, unsigned int *status, float *zstash, int grid,
                         bool beside, cudaStream_t stream);
 
