@@ -626,3 +626,104 @@ def test_prev_comb_table_is_the_scripts_output():
     w = synth.WORKLOADS["tiny"]
     _, _, _, pc = synth.tokens(w)
     assert all(any(np.array_equal(m, t) for t in stored) for m in pc)
+
+
+# ---------------------------------------------------------------- brute force, whole step
+
+def _mp_round_bf16(mp, x):
+    """x rounded to the nearest bf16 value (ties to even), computed in mpmath; also whether x
+    lies so close to a midpoint that a correctly rounded fp64 intermediate could round the other
+    way (such elements are left out of the exact comparison)."""
+    if x == 0:
+        return mp.mpf(0), False
+    a = abs(x)
+    e = int(mp.floor(mp.log(a, 2)))
+    while a >= mp.mpf(2) ** (e + 1):
+        e += 1
+    while a < mp.mpf(2) ** e:
+        e -= 1
+    assert -126 <= e <= 127, "normal bf16 range only"
+    ulp = mp.mpf(2) ** (e - 7)
+    q = x / ulp
+    n = mp.floor(q)
+    frac = q - n
+    if frac > mp.mpf(1) / 2 or (frac == mp.mpf(1) / 2 and int(n) % 2 == 1):
+        n += 1
+    near_tie = abs(frac - mp.mpf(1) / 2) < mp.mpf(10) ** -9
+    return n * ulp, near_tie
+
+
+def _mp_step(mp, R, Y, pp, pc, phi, bias, ms, gamma, sc):
+    """The definition's four steps for one token, term by term at 50 digits: bf16 inputs widened
+    exactly, R' and the layer input rounded to bf16, everything else unrounded."""
+    H = Y.shape[0]
+    f = lambda v: mp.mpf(float(v))
+    Rm = [[f(F(np.uint16(R[j, h]))) for h in range(H)] for j in range(4)]
+    Ym = [f(F(np.uint16(Y[h]))) for h in range(H)]
+    Rp, Rp_tie = [[None] * H for _ in range(4)], [[False] * H for _ in range(4)]
+    for i in range(4):
+        for h in range(H):
+            v = f(pp[i]) * Ym[h]
+            for j in range(4):
+                v += f(pc[j, i]) * Rm[j][h]
+            Rp[i][h], Rp_tie[i][h] = _mp_round_bf16(mp, v)
+    ss = mp.fsum(Rp[i][h] ** 2 for i in range(4) for h in range(H))
+    r = 1 / mp.sqrt(ss / (4 * H) + f(sc["hc_norm_eps"]))
+    z = [r * mp.fsum(Rp[i][h] * f(phi[i * H + h, n]) for i in range(4) for h in range(H)) for n in range(24)]
+    pre = [1 / (1 + mp.exp(-(f(ms[0]) * z[i] + f(bias[i])))) for i in range(4)]
+    post = [f(sc["hc_post_scale"]) / (1 + mp.exp(-(f(ms[1]) * z[4 + i] + f(bias[4 + i])))) for i in range(4)]
+    M = [[mp.exp(f(ms[2]) * z[8 + 4 * a + c] + f(bias[8 + 4 * a + c])) for c in range(4)] for a in range(4)]
+    eps = f(sc["sinkhorn_eps"])
+    for _ in range(sc["sinkhorn_iters"]):
+        for a in range(4):
+            s = mp.fsum(M[a]) + eps
+            M[a] = [m / s for m in M[a]]
+        for c in range(4):
+            s = mp.fsum(M[a][c] for a in range(4)) + eps
+            for a in range(4):
+                M[a][c] /= s
+    X = [mp.fsum(pre[i] * Rp[i][h] for i in range(4)) for h in range(H)]
+    rstd = 1 / mp.sqrt(mp.fsum(x * x for x in X) / H + f(sc["rmsnorm_eps"]))
+    out, out_tie = zip(*[_mp_round_bf16(mp, X[h] * rstd * f(F(np.uint16(gamma[h])))) for h in range(H)])
+    return dict(Rp=Rp, Rp_tie=Rp_tie, r=r, pre=pre, post=post, res=M, X=list(out), X_tie=list(out_tie), rstd=rstd)
+
+
+@pytest.mark.parametrize("H,seed", [(8, 1), (8, 2), (16, 3), (16, 4)])
+def test_whole_step_matches_a_50_digit_brute_force(H, seed):
+    """The fp64 oracle against the step recomputed term by term in 50-digit arithmetic (mpmath),
+    with its own bf16 rounding: R' and the layer input equal bit for bit (barring values within
+    1e-9 of a bf16 midpoint, where the fp64 sum may round the other way), r, rstd and the mixes
+    within 1e-12.  Nothing of the oracle's code is reused; the inputs have larger alphas than the
+    workloads so that every logit moves its head."""
+    mpmath = pytest.importorskip("mpmath")
+    mp = mpmath.mp
+    mp.dps = 50
+    rng = np.random.default_rng([seed, 99])
+    R = bf(rng.standard_normal((1, 4, H)))
+    Y = bf(rng.standard_normal((1, H)))
+    pp = (2.0 / (1.0 + np.exp(-rng.standard_normal((1, 4))))).astype(np.float32)
+    pc = synth.prev_comb_table()[rng.integers(0, 1024, size=1)]
+    phi = (rng.standard_normal((4 * H, 24)) * 0.3).astype(np.float32)
+    bias = (rng.standard_normal(24) * 0.1).astype(np.float32)
+    ms = np.array([0.7, 0.5, 0.3], np.float32)
+    gamma = bf(1.0 + 0.1 * rng.standard_normal(H))
+    got = oracle.shifted_post_pre(R, Y, pp, pc, phi, bias, ms, gamma, **SC, debug=True)
+    ref = _mp_step(mp, R[0], Y[0], pp[0], pc[0], phi, bias, ms, gamma, SC)
+    ties = 0
+    for i in range(4):
+        for h in range(H):
+            if ref["Rp_tie"][i][h]:
+                ties += 1
+                continue
+            assert got["R"][0, i, h] == bf(float(ref["Rp"][i][h])), (i, h)
+    for h in range(H):
+        if ref["X_tie"][h]:
+            ties += 1
+            continue
+        assert got["X"][0, h] == bf(float(ref["X"][h])), h
+    assert ties <= 2
+    assert abs(got["r"][0] - float(ref["r"])) <= 1e-12 * float(ref["r"])
+    assert abs(got["rstd"][0] - float(ref["rstd"])) <= 1e-12 * float(ref["rstd"])
+    assert np.abs(got["pre"][0] - np.array([float(v) for v in ref["pre"]])).max() <= 1e-12
+    assert np.abs(got["post"][0] - np.array([float(v) for v in ref["post"]])).max() <= 1e-12
+    assert np.abs(got["res"][0] - np.array([[float(v) for v in row] for row in ref["res"]])).max() <= 1e-12
