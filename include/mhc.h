@@ -110,12 +110,13 @@ typedef enum mhc_schedule {
     MHC_SCHEDULE_BCAST = 10,      /* mhc_pre_broadcast only (H % 64 == 0): one persistent kernel that
                                      works from x alone, 8 tokens per tile, x read twice (the second
                                      time from L2); the other calls choose as AUTO */
-    MHC_SCHEDULE_TILE = 11        /* H % 64 == 0, no MXFP8 output: one CTA per SM on tiles of 16 tokens,
-                                     no clusters; a tile's row walked twice in chunks (post, R' to HBM
+    MHC_SCHEDULE_TILE = 11        /* H % 64 == 0, H > 256: one CTA per SM on tiles of 18 tokens, no
+                                     clusters; a tile's row walked twice in chunks (post, R' to HBM
                                      and kept in L2, projection with phi read from L2; then the
-                                     combine from R' read back).  AUTO runs it beside ws on the SMs
-                                     that ws's clusters leave idle, on a share of the tokens, for
-                                     calls of at least 2048 tokens; forced, it takes every SM */
+                                     combine from R' read back, with the MXFP8 form when asked for).
+                                     AUTO runs it beside ws on the SMs that ws's clusters leave idle,
+                                     on a share of the tokens (mhc_auto_side_tokens), for calls of
+                                     at least 2048 tokens; forced, it takes every SM */
 } mhc_schedule;
 
 /* Bytes of workspace the calls below need for T tokens of hidden size H. */

@@ -87,7 +87,7 @@ cudaError_t launch_ws(const FusedArgs &a, unsigned int *status, float *zstash, c
 // CTAs of ws resident at once on this device (clusters of 16 that fit, times 16).
 cudaError_t ws_resident_ctas(int H, bool post, int &ctas);
 
-// Token-tile schedule (kernels_tile.cu): tiles of 16 tokens, one CTA per SM, no clusters; phi
+// Token-tile schedule (kernels_tile.cu): tiles of 18 tokens, one CTA per SM, no clusters; phi
 // read from the ws packed form (a.phi_pack).  It computes tokens [t_begin, a.T) with up to
 // `grid` CTAs, alone or beside ws (beside: launched right after ws on the same stream, on the
 // SMs ws leaves idle).  The tokens whose streams cancel in X go on the redo list.
