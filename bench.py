@@ -239,8 +239,7 @@ def run_ours(args, rank, world, lr, dist):
     # phi is a weight: packed once (mhc_pack_phi), as at model load, and the fused call and the pre
     # take the packed form (mhc_*_prepacked, bit-identical to the plain calls); --pack-per-call
     # times the plain calls, which pack phi in their workspace on every call
-    packed = mhc.pack_phi(wd[0]) if args.op in ("fused", "pre") and args.mxfp8 == "none" and not args.pack_per_call \
-        else None
+    packed = mhc.pack_phi(wd[0]) if args.op in ("fused", "pre") and not args.pack_per_call else None
     out = {"residual_out": torch.empty((T, 4, H), dtype=torch.bfloat16, device=dev),
            "layer_in": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
            "pre_mix": torch.empty((T, 4), device=dev), "post_mix": torch.empty((T, 4), device=dev),
@@ -325,7 +324,7 @@ def run_ours(args, rank, world, lr, dist):
         else:
             mhc.shifted_post_pre_mxfp8(R_, Y_, pp_, pc_, *wd, **sc, scale_mode=mx_mode,
                                        out=dict(o, layer_in=None) if args.no_bf16 else o, workspace=ws,
-                                       want_bf16=not args.no_bf16, stream=st)
+                                       want_bf16=not args.no_bf16, stream=st, packed_phi=packed)
 
     def step():
         call(Rd, Yd, ppd, pcd)

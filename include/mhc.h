@@ -315,6 +315,16 @@ MHC_API mhc_status mhc_pre_prepacked(const mhc_bf16 *residual, const float *phi,
                                      mhc_bf16 *layer_in_out, float *pre_mix_out, float *post_mix_out,
                                      float *comb_res_mix_out, void *workspace, size_t workspace_bytes,
                                      void *stream);
+/* mhc_shifted_post_pre_mxfp8 with the packed phi (arguments as there, packed_phi after phi);
+ * bit-identical to it. */
+MHC_API mhc_status mhc_shifted_post_pre_mxfp8_prepacked(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
+    const float *prev_comb_res_mix, const float *phi, const void *packed_phi, const float *bias,
+    const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps,
+    float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out,
+    mhc_bf16 *layer_in_out, uint8_t *layer_in_fp8, uint8_t *layer_in_scales, int scale_mode,
+    float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out, void *workspace,
+    size_t workspace_bytes, void *stream);
 
 /* The first layer's pre: the residual does not exist yet and the layer's (T, H) input x is
  * broadcast to the four streams ("[DSv4.1] Integrate Mega-mHC from DeepGEMM", "Paths on current

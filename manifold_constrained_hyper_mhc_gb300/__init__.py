@@ -79,6 +79,9 @@ def lib():
             L.mhc_shifted_post_pre_prepacked.restype = I
             L.mhc_pre_prepacked.argtypes = [P, P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
             L.mhc_pre_prepacked.restype = I
+            L.mhc_shifted_post_pre_mxfp8_prepacked.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, F, F, F, F, I,
+                                                               P, P, P, P, I, P, P, P, P, Z, P]
+            L.mhc_shifted_post_pre_mxfp8_prepacked.restype = I
             L.mhc_post.argtypes = [P, P, P, P, I64, I64, P, P]
             L.mhc_post.restype = I
             L.mhc_pre.argtypes = [P, P, P, P, P, I64, I64, F, F, F, F, I, P, P, P, P, P, Z, P]
@@ -260,10 +263,11 @@ def mxfp8_scale_bytes(T: int, H: int) -> int:
 def shifted_post_pre_mxfp8(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
                            rmsnorm_weight, *, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
                            sinkhorn_iters=20, scale_mode=MX_SCALE_FLOOR, want_bf16=True, out=None,
-                           workspace=None, stream=None):
+                           workspace=None, stream=None, packed_phi=None):
     """mhc_shifted_post_pre_mxfp8: the fused step with the layer input also as MXFP8.  Returns the
     dict of shifted_post_pre (layer_in only if want_bf16) plus layer_in_fp8 [T,H] uint8 (E4M3
-    codes) and layer_in_scales (uint8, mxfp8_scale_bytes(T, H), 128x4 tile layout)."""
+    codes) and layer_in_scales (uint8, mxfp8_scale_bytes(T, H), 128x4 tile layout).  With
+    packed_phi (pack_phi's output for this phi) it calls mhc_shifted_post_pre_mxfp8_prepacked."""
     torch = _torch()
     T, _, H = residual.shape
     _bf16(residual, "residual", (T, 4, H)); _bf16(layer_out, "layer_out", (T, H))
@@ -280,14 +284,18 @@ def shifted_post_pre_mxfp8(residual, layer_out, prev_post_mix, prev_comb_res_mix
     if "layer_in_scales" not in o:
         o["layer_in_scales"] = torch.empty(max(mxfp8_scale_bytes(T, H), 1), dtype=torch.uint8, device=dev)
     ws = workspace if workspace is not None else new_workspace(T, H, dev)
-    rc = lib().mhc_shifted_post_pre_mxfp8(
-        _ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi),
-        _ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
-        hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
-        _ptr(o["layer_in_fp8"]), _ptr(o["layer_in_scales"]), int(scale_mode), _ptr(o["pre_mix"]),
-        _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws), ws.numel() * ws.element_size(),
-        _stream(stream, dev))
-    _check(rc, "mhc_shifted_post_pre_mxfp8")
+    head = (_ptr(residual), _ptr(layer_out), _ptr(prev_post_mix), _ptr(prev_comb_res_mix), _ptr(phi))
+    tail = (_ptr(bias), _ptr(mix_scales), _ptr(rmsnorm_weight), T, H, hc_norm_eps, rmsnorm_eps,
+            hc_post_scale, sinkhorn_eps, int(sinkhorn_iters), _ptr(o["residual_out"]), _ptr(o["layer_in"]),
+            _ptr(o["layer_in_fp8"]), _ptr(o["layer_in_scales"]), int(scale_mode), _ptr(o["pre_mix"]),
+            _ptr(o["post_mix"]), _ptr(o["comb_res_mix"]), _ptr(ws), ws.numel() * ws.element_size(),
+            _stream(stream, dev))
+    if packed_phi is None:
+        rc = lib().mhc_shifted_post_pre_mxfp8(*head, *tail)
+        _check(rc, "mhc_shifted_post_pre_mxfp8")
+    else:
+        rc = lib().mhc_shifted_post_pre_mxfp8_prepacked(*head, _ptr(packed_phi), *tail)
+        _check(rc, "mhc_shifted_post_pre_mxfp8_prepacked")
     return o
 
 

@@ -650,6 +650,23 @@ mhc_status mhc_shifted_post_pre_prepacked(const mhc_bf16 *residual, const mhc_bf
                         packed_phi);
 }
 
+mhc_status mhc_shifted_post_pre_mxfp8_prepacked(
+    const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix, const float *prev_comb_res_mix,
+    const float *phi, const void *packed_phi, const float *bias, const float *mix_scales,
+    const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H, float hc_norm_eps, float rmsnorm_eps, float hc_post_scale,
+    float sinkhorn_eps, int sinkhorn_iters, mhc_bf16 *residual_out, mhc_bf16 *layer_in_out, uint8_t *layer_in_fp8,
+    uint8_t *layer_in_scales, int scale_mode, float *pre_mix_out, float *post_mix_out, float *comb_res_mix_out,
+    void *workspace, size_t workspace_bytes, void *stream) {
+    g_launches = 0;
+    if (packed_phi == nullptr && T > 0) return fail(MHC_ERR_INVALID_ARG, "packed_phi is NULL");
+    if (layer_in_fp8 == nullptr && T > 0) return fail(MHC_ERR_INVALID_ARG, "layer_in_fp8 is NULL");
+    return run_post_pre(residual, layer_out, prev_post_mix, prev_comb_res_mix, phi, bias, mix_scales,
+                        rmsnorm_weight, T, H, hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps,
+                        sinkhorn_iters, residual_out, layer_in_out, pre_mix_out, post_mix_out,
+                        comb_res_mix_out, workspace, workspace_bytes, stream, true, layer_in_fp8,
+                        layer_in_scales, scale_mode, nullptr, packed_phi);
+}
+
 mhc_status mhc_pre_prepacked(const mhc_bf16 *residual, const float *phi, const void *packed_phi, const float *bias,
                              const float *mix_scales, const mhc_bf16 *rmsnorm_weight, int64_t T, int64_t H,
                              float hc_norm_eps, float rmsnorm_eps, float hc_post_scale, float sinkhorn_eps,

@@ -75,3 +75,23 @@ def test_pack_phi_equals_the_workspace_packing(mhc):
     n = mhc.packed_phi_bytes(w.H)
     torch.cuda.synchronize()
     assert torch.equal(ws[256:256 + n], packed[:n])
+
+
+@pytest.mark.parametrize("schedule,T,H,want_bf16", [("auto", 8192, 7168, True), ("auto", 8192, 7168, False),
+                                                    ("auto", 6, 7168, True), ("ws", 130, 4096, False),
+                                                    ("tile", 300, 4096, True)])
+def test_mxfp8_prepacked_equals_plain(mhc, schedule, T, H, want_bf16):
+    """mhc_shifted_post_pre_mxfp8_prepacked: every output bit-identical to the plain MXFP8 call."""
+    w = synth.Workload(f"mxpk_{T}x{H}", T, H, 77)
+    tok, wts = _args(w)
+    mhc.set_schedule(schedule)
+    try:
+        nsb = mhc.mxfp8_scale_bytes(T, H)
+        zeros = lambda: {"layer_in_scales": torch.zeros(nsb, dtype=torch.uint8, device="cuda")}
+        a = mhc.shifted_post_pre_mxfp8(*tok, *wts, **SC, want_bf16=want_bf16, out=zeros())
+        b = mhc.shifted_post_pre_mxfp8(*tok, *wts, **SC, want_bf16=want_bf16, out=zeros(),
+                                       packed_phi=mhc.pack_phi(wts[0]))
+        torch.cuda.synchronize()
+    finally:
+        mhc.set_schedule("auto")
+    _same({k: v for k, v in a.items() if v is not None}, {k: v for k, v in b.items() if v is not None})
