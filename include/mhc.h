@@ -92,7 +92,8 @@ typedef enum mhc_status {
 typedef enum mhc_schedule {
     MHC_SCHEDULE_AUTO = 0,
     MHC_SCHEDULE_SPLIT = 1,       /* three launches: post + partial sums, mixes, combine + RMSNorm
-                                     (any H; AUTO's choice where ws does not fit, H > 7168) */
+                                     (any H; AUTO's choice where ws does not fit, H > 7168, for
+                                     T < 448; from 448 tokens AUTO takes the tile schedule there) */
     /* values 2-7 named cluster and pipelined schedules that the ws schedule superseded; they
        were removed and mhc_set_schedule rejects them */
     MHC_SCHEDULE_WS = 8,          /* clusters of 16 CTAs split the hidden dimension (H <= 7168), 8
@@ -199,12 +200,14 @@ MHC_API size_t mhc_mxfp8_scale_bytes(int64_t T, int64_t H);
  *                     GEMMs); padding bytes (m >= T, k >= H/32) are not written
  *   scale_mode        MHC_MX_SCALE_FLOOR or MHC_MX_SCALE_CEIL; E is clamped to [-127, 127],
  *                     and an all-zero block gets E = -127
- * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  Runs on the ws (with the tile kernel
- * beside it, as AUTO splits a plain call), tile and small schedules; a forced split schedule
- * returns MHC_ERR_UNSUPPORTED.  On ws with layer_in_out given, the quantize is a second
- * streaming pass over the bf16 layer input (the same bits; cheaper there than the in-kernel
- * epilogue).  The bf16 output and the mixes are bit-identical to mhc_shifted_post_pre's with the
- * same schedule setting. */
+ * Needs H % 32 == 0 (MHC_ERR_INVALID_ARG otherwise).  The ws (with the tile kernel beside it,
+ * as AUTO splits a plain call), tile and small schedules quantize in their combine epilogue, or,
+ * on ws and tile with layer_in_out given, in a second streaming pass over the bf16 layer input
+ * (the same bits; cheaper there than the epilogue).  The split schedule always takes the second
+ * pass; with layer_in_out NULL it first writes the bf16 layer input into the workspace, which
+ * mhc_workspace_size reserves where AUTO can choose split (H > 7168, T < 448); a forced split
+ * call elsewhere then returns MHC_ERR_WORKSPACE when the workspace is too small.  The bf16 output
+ * and the mixes are bit-identical to mhc_shifted_post_pre's with the same schedule setting. */
 MHC_API mhc_status mhc_shifted_post_pre_mxfp8(
     const mhc_bf16 *residual, const mhc_bf16 *layer_out, const float *prev_post_mix,
     const float *prev_comb_res_mix, const float *phi, const float *bias, const float *mix_scales,

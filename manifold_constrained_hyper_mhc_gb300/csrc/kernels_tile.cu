@@ -1,5 +1,5 @@
 // Token-tile schedule (schedule "tile"): the whole fused mHC post+pre step for tiles of 18
-// tokens, one CTA per SM, no clusters.  It runs on its own (every SM, any H % 64 == 0), or
+// tokens, one CTA per SM, no clusters.  It runs on its own (every SM, H % 64 == 0, H > 256), or
 // beside the ws schedule on the SMs that ws's 16-CTA clusters cannot use, on a share of the
 // tokens (ws takes the leading tokens, this kernel the rest).
 //

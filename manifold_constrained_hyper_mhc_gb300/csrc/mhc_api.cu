@@ -94,8 +94,26 @@ mhc_status current_device(Device &d) {
     return MHC_OK;
 }
 
+// Beyond ws's hidden size (H > 7168) the token-tile kernel alone beats the split schedule from
+// about this many tokens: one round of its tiles costs about 100-110 us at H = 7232-8192, the
+// split schedule about 0.23-0.25 us per token (graph-replayed: T = 512, H = 8192: 111.5 vs
+// 152.8 us; T = 128: 110.1 vs 46.0 us; T = 8192: 410 vs 2,032 us).
+constexpr int64_t kTileAloneMinT = 448;
+
+// The split schedule's MXFP8-only call quantizes a bf16 layer input that it first writes here,
+// after the split scratch.  Only reserved where AUTO can choose split (a forced split call with a
+// larger T and no bf16 output is refused when the workspace has no room).
+size_t split_mx_scratch_offset(int64_t T, int64_t H) {
+    return mhc::kControlBytes + ((mhc::split_workspace_bytes(T, H) + 255) & ~size_t(255));
+}
+bool split_mx_scratch_reserved(int64_t T, int64_t H) {
+    return H >= 8 && H <= MHC_MAX_HIDDEN && !mhc::ws_supported((int)H) && T < kTileAloneMinT;
+}
+
 size_t workspace_bytes_for(int64_t T, int64_t H) {
     size_t sched = mhc::split_workspace_bytes(T, H);
+    if (split_mx_scratch_reserved(T, H))
+        sched = ((sched + 255) & ~size_t(255)) + (size_t)T * (size_t)H * 2;
     if (H >= 8 && H <= MHC_MAX_HIDDEN)
     {
         sched = std::max(sched, ((mhc::ws_pack_bytes((int)H) + 255) & ~size_t(255)) + mhc::ws_stash_bytes(T));
@@ -109,9 +127,11 @@ size_t workspace_bytes_for(int64_t T, int64_t H) {
 // Up to this many tokens the one-barrier small-T schedule has the lower latency.
 constexpr int64_t kSmallAutoMaxT = 32;
 
+
 int auto_schedule(int64_t T, int64_t H, int sms, bool mx = false) {
     if (T <= kSmallAutoMaxT && mhc::small_supported(T, (int)H, sms, mx)) return MHC_SCHEDULE_SMALL;
     if (mhc::ws_supported((int)H)) return MHC_SCHEDULE_WS;
+    if (mhc::tile_supported(T, H) && T >= kTileAloneMinT) return MHC_SCHEDULE_TILE;
     return MHC_SCHEDULE_SPLIT;
 }
 
@@ -229,8 +249,16 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
     mhc::Scalars s{hc_norm_eps, rmsnorm_eps, hc_post_scale, sinkhorn_eps, sinkhorn_iters};
     const int sched = choose_schedule(T, H, dev.sms, mx);
     const mhc::MxOut mxo{mx_q, mx_scale, mx_mode};
-    if (mx && sched != MHC_SCHEDULE_WS && sched != MHC_SCHEDULE_SMALL && sched != MHC_SCHEDULE_TILE)
-        return fail(MHC_ERR_UNSUPPORTED, "the MXFP8 output is produced by the ws, tile and small schedules only");
+    // the split schedule writes its bf16 layer input first (to the caller's buffer, or to the
+    // workspace when only the MXFP8 form is wanted) and quantizes it in a second pass
+    uint16_t *split_x = layer_in_out;
+    if (mx && sched == MHC_SCHEDULE_SPLIT && layer_in_out == nullptr) {
+        const size_t need = split_mx_scratch_offset(T, H) + (size_t)T * (size_t)H * 2;
+        if (workspace_bytes < need)
+            return fail(MHC_ERR_WORKSPACE, "the split schedule's MXFP8-only call needs %zu workspace bytes, got %zu",
+                        need, workspace_bytes);
+        split_x = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + split_mx_scratch_offset(T, H));
+    }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     switch (sched) {
@@ -240,11 +268,15 @@ mhc_status run_post_pre(const mhc_bf16 *residual, const mhc_bf16 *layer_out,
             a.phi = phi; a.bias = bias; a.mix_scales = mix_scales; a.gamma = rmsnorm_weight;
             a.T = T; a.H = (int)H; a.s = s;
             a.R_out = fused ? residual_out : nullptr;
-            a.X_out = layer_in_out; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
+            a.X_out = split_x; a.pre_out = pre_mix_out; a.post_out = post_mix_out;
             a.res_out = comb_res_mix_out;
             a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + mhc::kControlBytes);
             e = mhc::launch_split(a, cs);
             g_launches = 3;
+            if (e == cudaSuccess && mx) {
+                e = mhc::launch_mx_quantize(split_x, T, (int)H, mxo, dev.sms, cs);
+                g_launches += 1;
+            }
             break;
         }
         case MHC_SCHEDULE_WS:

@@ -94,7 +94,8 @@ def run_case(mhc, w, schedule, mode, gamma_decades=True, check_oracle=True):
     ("small", 6, 7168), ("small", 37, 1024), ("small", 1, 4096),
     ("ws", 6, 7168), ("ws", 130, 4096), ("ws", 300, 7168), ("ws", 9, 2080),
     ("tile", 40, 7168), ("tile", 300, 4096), ("tile", 7, 1088),
-    ("auto", 6, 7168), ("auto", 1000, 7168), ("auto", 2500, 7168)])
+    ("split", 40, 7168), ("split", 17, 1088),
+    ("auto", 6, 7168), ("auto", 1000, 7168), ("auto", 2500, 7168), ("auto", 40, 7232), ("auto", 500, 7232)])
 def test_mxfp8_epilogue_matches_separate_quantize(mhc, schedule, T, H, mode):
     run_case(mhc, synth.Workload(f"mx_{schedule}_{T}x{H}", T, H, 300 + T, token_scale=True), schedule, mode)
 
@@ -113,19 +114,21 @@ def test_mxfp8_rejects_bad_shapes_and_schedules(mhc):
     with pytest.raises(mhc.MhcError) as ei:
         mhc.shifted_post_pre_mxfp8(*args, **SC)
     assert ei.value.status == -1
-    w = synth.Workload("mx_split", 4, 1024, 6)
+    # a forced split call with the MXFP8 form only writes its bf16 layer input to the workspace
+    # first; where AUTO would not take split (H <= 7168 here) the workspace has no room for it
+    w = synth.Workload("mx_split", 600, 7168, 6)
     phi, bias, ms, gamma = synth.weights(w)
     R, Y, pp, pc = synth.tokens(w)
     args = (dev_bf16(R), dev_bf16(Y), dev_f32(pp), dev_f32(pc), dev_f32(phi), dev_f32(bias), dev_f32(ms),
             dev_bf16(gamma))
-    out = {"layer_in_fp8": torch.full((4, 1024), 7, dtype=torch.uint8, device="cuda")}
+    out = {"layer_in_fp8": torch.full((600, 7168), 7, dtype=torch.uint8, device="cuda")}
     mhc.set_schedule("split")
     try:
         with pytest.raises(mhc.MhcError) as ei:
-            mhc.shifted_post_pre_mxfp8(*args, **SC, out=out)
+            mhc.shifted_post_pre_mxfp8(*args, **SC, want_bf16=False, out=out)
     finally:
         mhc.set_schedule("auto")
-    assert ei.value.status == -2
+    assert ei.value.status == -3
     with pytest.raises(mhc.MhcError) as ei:
         mhc.shifted_post_pre_mxfp8(*args, **SC, scale_mode=2, out=out)
     assert ei.value.status == -1

@@ -84,9 +84,18 @@ def test_ragged_shapes(mhc, T, H, schedule):
 
 @pytest.mark.parametrize("T,H", [(1, 320), (17, 1088), (37, 2112), (130, 7168), (300, 4096), (1000, 7168)])
 def test_tile_schedule_shapes(mhc, T, H):
-    """The token-tile kernel alone on every SM: a single token, ragged tiles (T % 16 != 0) and
+    """The token-tile kernel alone on every SM: a single token, ragged tiles (T % 18 != 0) and
     ragged chunks (H % 256 != 0), more tiles than SMs."""
     check_workload(mhc, synth.Workload(f"tile_{T}x{H}", T, H, 200 + T, token_scale=True), "tile")
+
+
+@pytest.mark.parametrize("T,H", [(500, 7232), (600, 8192), (100, 7232), (40, 8256)])
+def test_auto_beyond_ws_hidden_size(mhc, T, H):
+    """H > 7168, where ws's 16-CTA slice no longer fits: AUTO takes the token-tile kernel alone
+    from 448 tokens on and the split schedule below; every token against the oracle."""
+    want = "tile" if T >= 448 else "split"
+    assert mhc.auto_schedule(T, H) == mhc.SCHEDULES[want]
+    check_workload(mhc, synth.Workload(f"wide_{T}x{H}", T, H, 400 + T, token_scale=True))
 
 
 @pytest.mark.parametrize("T,H", [(2048, 7168), (4096, 4096), (2500, 7168)])
