@@ -34,13 +34,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait.  After one timeout (`dead` set), later waits give up at once.
-__device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, bool &dead, uint32_t limit) {
-    const uint32_t n = dead ? 1u : limit;
-    for (uint32_t i = 0; i < n; ++i)
-        if (mbar_try_wait(bar, parity)) return;
-    dead = true;
-}
 // As mbar_try_wait, but an incomplete phase may suspend the thread for up to
 // hint_ns nanoseconds (it resumes earlier when the phase completes), so a
 // waiting warp takes far fewer issue slots than with back-to-back polls.
