@@ -75,7 +75,9 @@ typedef uint16_t mhc_bf16; /* bfloat16 bit pattern */
 
 #define MHC_HC_MULT 4
 #define MHC_NUM_MIX 24
-#define MHC_MAX_TOKENS (1 << 22)
+/* the 2^20-token bound of the integrated kernel ("[DSv4.1] Integrate Mega-mHC from DeepGEMM",
+ * Verified OK) */
+#define MHC_MAX_TOKENS (1 << 20)
 #define MHC_MAX_HIDDEN 65536
 #define MHC_MAX_SINKHORN_ITERS 64
 

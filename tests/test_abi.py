@@ -52,7 +52,7 @@ def _call_fused(L, T, H, ptrs=None, scal=(2e-5, 2e-6, 1.25, 3e-4, 20), ws_bytes=
     return L.mhc_shifted_post_pre(*p, T, H, *scal[:4], scal[4], *outs, _fake(ws), ws_bytes, None)
 
 
-@pytest.mark.parametrize("T,H", [(-1, 1024), (1 << 23, 1024), (4, 0), (4, 12), (4, 65544), (4, 4)])
+@pytest.mark.parametrize("T,H", [(-1, 1024), ((1 << 20) + 1, 1024), (1 << 23, 1024), (4, 0), (4, 12), (4, 65544), (4, 4)])
 def test_bad_sizes_are_rejected(mhc_lib, T, H):
     assert _call_fused(mhc_lib.lib(), T, H) == -1
 
