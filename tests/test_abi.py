@@ -115,3 +115,17 @@ def test_binding_fails_loudly_without_cuda(mhc_lib):
     with pytest.raises((ValueError, RuntimeError)):
         mhc_lib.post(x, torch.zeros((2, 64), dtype=torch.bfloat16), torch.zeros((2, 4)),
                      torch.zeros((2, 4, 4)))
+
+
+def test_planning_queries_without_a_device(mhc_lib):
+    """The AUTO planning queries need a current CUDA device; without one (this CPU machine) they say so
+    instead of guessing: the side share is -1, and bad sizes are -1 as well."""
+    L = mhc_lib.lib()
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a CUDA device is present")
+    except ImportError:
+        pass
+    assert mhc_lib.auto_side_tokens(8192, 7168) == -1
+    assert L.mhc_auto_side_tokens(-1, 7168, 1) == -1

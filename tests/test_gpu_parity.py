@@ -98,6 +98,17 @@ def test_auto_beyond_ws_hidden_size(mhc, T, H):
     check_workload(mhc, synth.Workload(f"wide_{T}x{H}", T, H, 400 + T, token_scale=True))
 
 
+def test_auto_side_share_query(mhc):
+    """mhc_auto_side_tokens: no side share below 2048 tokens or off the ws schedule, whole tiles
+    of the idle SMs above, the same share for the pre alone when its clusters fit the same SMs."""
+    assert mhc.auto_side_tokens(1024, 7168) == 0
+    assert mhc.auto_side_tokens(6, 7168) == 0
+    assert mhc.auto_side_tokens(8192, 8192) == 0           # H > 7168: tile alone, not beside ws
+    side = mhc.auto_side_tokens(8192, 7168)
+    assert 0 < side < 8192 and (8192 - side) % 8 == 0
+    assert mhc.auto_side_tokens(-1, 7168) == -1
+
+
 @pytest.mark.parametrize("T,H", [(2048, 7168), (4096, 4096), (2500, 7168)])
 def test_ws_with_tile_beside(mhc, T, H):
     """AUTO from 2048 tokens on: ws on the leading tokens, the token-tile kernel beside it on the
