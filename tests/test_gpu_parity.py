@@ -99,8 +99,8 @@ def test_auto_beyond_ws_hidden_size(mhc, T, H):
 
 
 def test_auto_side_share_query(mhc):
-    """mhc_auto_side_tokens: no side share below 2048 tokens or off the ws schedule, whole tiles
-    of the idle SMs above, the same share for the pre alone when its clusters fit the same SMs."""
+    """mhc_auto_side_tokens: no side share below 2048 tokens or off the ws schedule; above, ws
+    keeps a whole number of 8-token groups and the tile kernel the rest."""
     assert mhc.auto_side_tokens(1024, 7168) == 0
     assert mhc.auto_side_tokens(6, 7168) == 0
     assert mhc.auto_side_tokens(8192, 8192) == 0           # H > 7168: tile alone, not beside ws
