@@ -18,9 +18,11 @@
 //      shared memory and sums it over the CTAs in one fixed order, so all CTAs
 //      hold identical r, pre and rstd (sum_h X^2 = pre^T G pre);
 //   5. combine + RMSNorm of its slice from the R' in shared memory;
-//   meanwhile warp 0 of CTA c < T bulk-copies token c's other 20 logits, sums
-//   them, takes r and the pre logits from phase 4 and finishes its mixes (pre,
-//   post, Sinkhorn residual mix), so the Sinkhorn runs beside phase 5.
+//   meanwhile warp 0 of CTA c < T bulk-copies token c's other 20 logits and sums
+//   them; it takes r and the pre logits from phase 4 (below 16 tokens) or sums the
+//   token's heads itself in phase 4's order (the same bits, without waiting for
+//   phase 4's sums over every token), and finishes its mixes (pre, post, Sinkhorn
+//   residual mix), so the Sinkhorn runs beside phase 5.
 // phi is used in fp32 directly (no packing launch) and nothing is re-read from
 // HBM, so a call is a single launch.
 //
@@ -48,6 +50,9 @@ constexpr int kHead = 16, kTail = 24;  // floats per record head / tail
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
 constexpr int kBigBytes = 100 * 1024;  // shared memory for one token chunk of record heads
 constexpr size_t kSmallSmemLimit = 227 * 1024;
+// From this many tokens the owner warp sums its token's heads itself (graph-replayed, H = 7168:
+// T = 32 12.4 us against 14.0 us taking the workers' sums; T = 6 9.1 against 8.7 us).
+constexpr int kOwnHeadsMinT = 16;
 constexpr int kMaxCtas = 160;  // CTAs at most (one per SM)
 
 // Tokens per chunk of the phase-4 reduction (the heads of nc records each), at most 16.
@@ -76,7 +81,8 @@ struct SmallSmem {
     __host__ __device__ size_t ownt_off() const {  // [nc][24]
         return big_off() + (size_t)small_chunk(T, nc) * nc * kHead * 4;
     }
-    __host__ __device__ size_t sums_off() const { return ownt_off() + (size_t)nc * kTail * 4; }  // [T][16]
+    __host__ __device__ size_t ownh_off() const { return ownt_off() + (size_t)nc * kTail * 4; }  // [nc][16]
+    __host__ __device__ size_t sums_off() const { return ownh_off() + (size_t)nc * kHead * 4; }  // [T][16]
     __host__ __device__ size_t st_off() const { return sums_off() + (size_t)T * 16 * 4; }        // [T][8]
     __host__ __device__ size_t tl_off() const { return st_off() + (size_t)T * 8 * 4; }           // [32]
     __host__ __device__ size_t flag_off() const { return tl_off() + 32 * 4; }
@@ -163,6 +169,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
     float *sGram = reinterpret_cast<float *>(sm + L.gram_off());
     float *sBig = reinterpret_cast<float *>(sm + L.big_off());
     float *sOwnT = reinterpret_cast<float *>(sm + L.ownt_off());
+    float *sOwnH = reinterpret_cast<float *>(sm + L.ownh_off());
     float *sSums = reinterpret_cast<float *>(sm + L.sums_off());
     float *sSt = reinterpret_cast<float *>(sm + L.st_off());
     float *sTl = reinterpret_cast<float *>(sm + L.tl_off());
@@ -356,28 +363,48 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
 
     // split: no owner warps; the post and residual mixes are left to small_tail_kernel
     const bool owner_cta = !split && c < T;
+    // the owner warp sums its token's heads itself from kOwnHeadsMinT tokens on; with fewer, the
+    // workers' sums over every token are done sooner than its own copy, and it takes theirs
+    const bool own_heads = T >= kOwnHeadsMinT;
     if (owner_cta && warp == 0) {
-        // ---- token c (and c + nc, ...): logits 4..23 summed over the CTAs; pre logits and r from
-        // the workers' sums; heads and the Sinkhorn mix.
+        // ---- token c (and c + nc, ...): its records summed over the CTAs here (the heads in the
+        // workers' order and arithmetic, so r and the pre logits are the same bits as theirs,
+        // without waiting for their sums over every token); heads and the Sinkhorn mix.
         int it = 0;
         for (int t = c; t < T; t += nc, ++it) {
             if (lane == 0) {
                 fence_proxy_async_global();
                 if (it > 0) fence_proxy_async_smem();  // the previous token's reads of the buffer are done
-                mbar_arrive_expect_tx(&bars[3], nc * kTail * 4u);
+                mbar_arrive_expect_tx(&bars[3], nc * (own_heads ? kTail + kHead : kTail) * 4u);
                 bulk_g2s(sOwnT, tails + (size_t)t * nc * kTail, nc * kTail * 4u, &bars[3]);
+                if (own_heads) bulk_g2s(sOwnH, heads + (size_t)t * nc * kHead, nc * kHead * 4u, &bars[3]);
             }
             mbar_wait_timed(&bars[3], it & 1, dead, kSpinLimitNs);
+            float zpre = 0.f, r = 0.f;
             {
                 const float4 a = warp_cta_sum16(sOwnT, kTail, nc, 4);       // logits 4..19
                 const float4 b = warp_cta_sum16(sOwnT + 16, kTail, nc, 1);  // logits 20..23
                 if (lane < 4) *reinterpret_cast<float4 *>(sTl + 4 * lane) = a;
                 if (lane == 0) *reinterpret_cast<float4 *>(sTl + 16) = b;
+                if (own_heads) {
+                    // lane j holds quad j: pre logits (quad 0), Gram diagonal (quad 1)
+                    const float4 h = warp_cta_sum16(sOwnH, kHead, nc, 2);
+                    const float g0 = __shfl_sync(0xffffffffu, h.x, 1), g1 = __shfl_sync(0xffffffffu, h.y, 1),
+                                g2 = __shfl_sync(0xffffffffu, h.z, 1), g3 = __shfl_sync(0xffffffffu, h.w, 1);
+                    r = hc_rsqrt((g0 + g1) + (g2 + g3), H, sc.hc_norm_eps);
+                    const float p0 = __shfl_sync(0xffffffffu, h.x, 0), p1 = __shfl_sync(0xffffffffu, h.y, 0),
+                                p2 = __shfl_sync(0xffffffffu, h.z, 0), p3 = __shfl_sync(0xffffffffu, h.w, 0);
+                    zpre = lane == 0 ? p0 : (lane == 1 ? p1 : (lane == 2 ? p2 : p3));
+                }
             }
             __syncwarp();
             const float tl = lane >= 4 && lane < kNumMix ? sTl[lane - 4] : 0.f;  // lane n: logit n
-            if (it == 0) asm volatile("bar.sync 2, %0;" ::"r"(kSNT) : "memory");  // workers' sums are in
-            const float z = sSt[t * 8 + 5] * (lane < 4 ? sSums[t * 16 + lane] : tl);
+            if (!own_heads) {
+                if (it == 0) asm volatile("bar.sync 2, %0;" ::"r"(kSNT) : "memory");  // workers' sums are in
+                r = sSt[t * 8 + 5];
+                zpre = lane < 4 ? sSums[t * 16 + lane] : 0.f;
+            }
+            const float z = r * (lane < 4 ? zpre : tl);
             const float v = heads_and_sinkhorn(z, bias, mix_scales, sc);
             if (lane < 4) pre_out[(size_t)t * 4 + lane] = v;
             else if (lane < 8) post_out[(size_t)t * 4 + lane - 4] = v;
@@ -437,7 +464,7 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         if (split && c == 0) *reinterpret_cast<float4 *>(pre_out + (size_t)t * 4) = make_float4(pre[0], pre[1], pre[2], pre[3]);
     }
     wsync();
-    if (owner_cta) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums and stats -> owner warp
+    if (owner_cta && !own_heads) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums -> owner warp
 
     // ---- 4b. tokens whose streams cancel in X (gram_cancels): sum_h X^2 summed directly.  Every
     // CTA flags the same tokens (it holds the same sums), so all of them take this branch or
