@@ -19,10 +19,11 @@
 //      hold identical r, pre and rstd (sum_h X^2 = pre^T G pre);
 //   5. combine + RMSNorm of its slice from the R' in shared memory;
 //   meanwhile warp 0 of CTA c < T bulk-copies token c's other 20 logits and sums
-//   them; it takes r and the pre logits from phase 4 (below 16 tokens) or sums the
-//   token's heads itself in phase 4's order (the same bits, without waiting for
-//   phase 4's sums over every token), and finishes its mixes (pre, post, Sinkhorn
-//   residual mix), so the Sinkhorn runs beside phase 5.
+//   them; below 16 tokens it computes r and takes the pre logits from phase 4's sums
+//   (signalled as soon as they are in, before the workers' rstd), from 16 tokens it
+//   sums the token's heads itself in phase 4's order (the same bits, without waiting
+//   for phase 4's sums over every token); then it finishes its mixes (pre, post,
+//   Sinkhorn residual mix), so the Sinkhorn runs beside phase 5.
 // phi is used in fp32 directly (no packing launch) and nothing is re-read from
 // HBM, so a call is a single launch.
 //
@@ -401,8 +402,10 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
             const float tl = lane >= 4 && lane < kNumMix ? sTl[lane - 4] : 0.f;  // lane n: logit n
             if (!own_heads) {
                 if (it == 0) asm volatile("bar.sync 2, %0;" ::"r"(kSNT) : "memory");  // workers' sums are in
-                r = sSt[t * 8 + 5];
-                zpre = lane < 4 ? sSums[t * 16 + lane] : 0.f;
+                // r as the workers compute it, from the same sums (the same bits)
+                const float *sm16 = sSums + t * 16;
+                r = hc_rsqrt((sm16[4] + sm16[5]) + (sm16[6] + sm16[7]), H, sc.hc_norm_eps);
+                zpre = lane < 4 ? sm16[lane] : 0.f;
             }
             const float z = r * (lane < 4 ? zpre : tl);
             const float v = heads_and_sinkhorn(z, bias, mix_scales, sc);
@@ -440,6 +443,8 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
             wsync();
         }
     }
+    // the owner warp needs only these sums (r and the pre logits), not the workers' rstd below
+    if (owner_cta && !own_heads) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums -> owner warp
     // r, pre and rstd of every token, one thread per token (identical in every CTA)
     for (int t = wt; t < T; t += nwork) {
         const float *s = sSums + t * 16;
@@ -457,14 +462,12 @@ small_kernel(const uint16_t *__restrict__ R, const uint16_t *__restrict__ Y, con
         const float rstd = 1.f / sqrtf(fmaxf(sx, 0.f) / (float)H + sc.rmsnorm_eps);
         *reinterpret_cast<float4 *>(sSt + t * 8) = make_float4(pre[0], pre[1], pre[2], pre[3]);
         sSt[t * 8 + 4] = rstd;
-        sSt[t * 8 + 5] = r;
         const bool fix = gram_cancels(sx, pre, G);
         sSt[t * 8 + 6] = fix ? 1.f : 0.f;
         if (fix) atomicAdd(&sFlag[1], 1);
         if (split && c == 0) *reinterpret_cast<float4 *>(pre_out + (size_t)t * 4) = make_float4(pre[0], pre[1], pre[2], pre[3]);
     }
     wsync();
-    if (owner_cta && !own_heads) asm volatile("bar.arrive 2, %0;" ::"r"(kSNT) : "memory");  // sums -> owner warp
 
     // ---- 4b. tokens whose streams cancel in X (gram_cancels): sum_h X^2 summed directly.  Every
     // CTA flags the same tokens (it holds the same sums), so all of them take this branch or
