@@ -409,7 +409,8 @@ def run_ours(args, rank, world, lr, dist):
             step()
         mhc.set_main_kernel_events(None, None)
     torch.cuda.synchronize(dev)
-    kernel_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in kev]))
+    span_each = np.array([a_.elapsed_time(b_) for a_, b_ in kev]) * 1e3  # us, one per call
+    kernel_ms = float(np.mean(span_each)) / 1e3
     el_ms = max_over_ranks(el_ms, dist, dev)
     ms_step = el_ms / args.steps
     value = world * T / (ms_step / 1e3)
@@ -578,6 +579,8 @@ def run_ours(args, rank, world, lr, dist):
                                + f", algorithmic bytes {abytes} per call"},
         "gpu_launches": launches * args.steps,
         "launch_mode": f"CUDA graph of {args.graph} calls, replayed" if args.graph > 0 else "eager",
+        "main_span_us": {"calls": int(span_each.size), "p10": float(np.percentile(span_each, 10)),
+                         "p50": float(np.percentile(span_each, 50)), "p90": float(np.percentile(span_each, 90))},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipelining": "two buffer sets; copies in, calls and copies out on three streams"},

@@ -37,6 +37,8 @@ def test_bench_line_has_the_contract_keys(extra):
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["config"]["T"] == 6 and d["config"]["H"] == 7168
+    sp = d["main_span_us"]
+    assert sp["calls"] >= 3 and 0 < sp["p10"] <= sp["p50"] <= sp["p90"]
 
 
 def test_bench_cpu_baseline_leg():
