@@ -309,10 +309,12 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
         walk(my_tiles, nch, lag, [&](int k, int pass, int c, int seq) {
             const int slot = seq % kNSlot;
             const uint32_t ph = (uint32_t)((seq / kNSlot) & 1);
+            const int h = c * kCW + v * kVec;
+            // pass 2: this lane's 8 values of gamma, loaded before the wait for the slot
+            const uint4 gv = pass == 1 && h < H ? ld_ro(gamma + h) : make_uint4(0u, 0u, 0u, 0u);
             bwait(&full[slot], ph, dead);
             unsigned char *sl = ring + (size_t)slot * kSlot;
             const int64_t t0 = tile_t0(k);
-            const int h = c * kCW + v * kVec;
             if (pass == 0) {
                 if (kPost && c == 0) bwait(&mixfull[k & 1], (uint32_t)((k >> 1) & 1), dead);
                 const float *mx = reinterpret_cast<const float *>(mixb + (size_t)(k & 1) * kMixB);
@@ -404,7 +406,7 @@ tile_kernel(const __grid_constant__ TileMaps maps, const uint4 *__restrict__ pac
                         for (int j = 0; j < kHC; ++j)
                             unpack8(*reinterpret_cast<const uint4 *>(sl + swz((j * kCHB + hb) * kTT + t, c16)), rf[j]);
                         combine_vec8_x2(rf, hp[u], x);
-                        ob = norm_vec8(x, hr[u], ld_ro(gamma + h));
+                        ob = norm_vec8(x, hr[u], gv);
                         if (X_out != nullptr) st_stream(X_out + (t0 + t) * (int64_t)H + h, ob);
                     }
                     // MXFP8 layer input: lanes 4a .. 4a+3 hold the block of 32 values a of the chunk

@@ -340,14 +340,21 @@ ws_kernel(const __grid_constant__ WsMaps maps, const uint4 *__restrict__ phi_pac
         tq = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col0;
         const uint4 *pack = phi_pack + (size_t)c * (kHC * Hs / 16) * 96;
         for (int i = 0; i < nblk(p); ++i) {
+            // the block's 12 fragment loads in flight together (a tensor-memory store orders memory,
+            // so loads issued after one wait for it)
+            uint4 fa[kHC][3];
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
                 const int s = j * nB16 + blk0(p) + i;
+#pragma unroll
+                for (int mt = 0; mt < 3; ++mt) fa[j][mt] = __ldg(pack + ((size_t)s * 3 + mt) * 32 + lane);
+            }
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) {
                 uint32_t r[16];
 #pragma unroll
                 for (int mt = 0; mt < 3; ++mt) {
-                    const uint4 a = __ldg(pack + ((size_t)s * 3 + mt) * 32 + lane);
-                    r[4 * mt] = a.x; r[4 * mt + 1] = a.y; r[4 * mt + 2] = a.z; r[4 * mt + 3] = a.w;
+                    r[4 * mt] = fa[j][mt].x; r[4 * mt + 1] = fa[j][mt].y; r[4 * mt + 2] = fa[j][mt].z; r[4 * mt + 3] = fa[j][mt].w;
                 }
                 r[12] = r[13] = r[14] = r[15] = 0u;
                 tmem_st16(tq + (uint32_t)((i * 4 + j) * 16), r);
